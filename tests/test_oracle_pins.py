@@ -1,0 +1,239 @@
+"""Pins of the fp64 oracle against things other than itself.
+
+Each test ties one step of the oracle to a closed form, a library routine, a
+brute-force computation written independently here, an invariant, or the
+hand-derived example in tests/golden/hand_example.txt. The steps are those of
+"MiTA Attention: Efficient Fast-Weight Scaling via a Mixture of Top-k
+Activations" (gist.science summaries: Arabic edition section 2 for pooling,
+shared expert and top-k sets; Dutch edition "Wiskundige Formulering" for the
+concatenated K* / V*; "Complexiteit" for the O(N(m + ks)) cost).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+# ---------------------------------------------------------------- pooling
+
+@pytest.mark.parametrize("N,m", [(64, 8), (100, 7), (33, 33), (10, 1), (1000, 16)])
+def test_pool_1d_matches_torch_adaptive_avg_pool(N, m):
+    Q = _rand((2, N, 5), 1)
+    got = oracle.pool(Q, m)
+    ref = torch.nn.functional.adaptive_avg_pool1d(torch.from_numpy(Q).transpose(1, 2), m)
+    np.testing.assert_allclose(got, ref.transpose(1, 2).numpy(), rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("gh,gw,lh,lw", [(16, 16, 4, 4), (12, 10, 5, 3), (8, 8, 8, 8), (6, 9, 1, 2)])
+def test_pool_2d_matches_torch_adaptive_avg_pool(gh, gw, lh, lw):
+    d = 3
+    Q = _rand((1, gh * gw, d), 2)
+    got = oracle.pool(Q, lh * lw, grid=(gh, gw), lm=(lh, lw))
+    img = torch.from_numpy(Q[0]).reshape(gh, gw, d).permute(2, 0, 1)[None]
+    ref = torch.nn.functional.adaptive_avg_pool2d(img, (lh, lw))[0].permute(1, 2, 0).reshape(lh * lw, d)
+    np.testing.assert_allclose(got[0], ref.numpy(), rtol=1e-13, atol=1e-13)
+
+
+def test_pool_divisible_is_window_mean():
+    Q = _rand((1, 96, 4), 3)
+    np.testing.assert_allclose(oracle.pool(Q, 12)[0], Q[0].reshape(12, 8, 4).mean(axis=1), rtol=1e-13)
+
+
+# -------------------------------------------------------- hand example
+
+def _golden():
+    vals = {}
+    with open(os.path.join(GOLDEN, "hand_example.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            name, *rest = line.split()
+            vals[name] = np.array([float(x) for x in rest])
+    return vals
+
+
+def test_hand_example():
+    g = _golden()
+    Q = np.array([0.0, 0.0, 1.0, 1.0]).reshape(1, 4, 1)
+    K = np.array([0.0, 0.0, math.log(3.0), 0.0]).reshape(1, 4, 1)
+    V = np.array([1.0, 2.0, 3.0, 4.0]).reshape(1, 4, 1)
+    r = oracle.forward(Q, K, V, m=2, k=1, s=1, scale=1.0, threads=1)
+    np.testing.assert_allclose(r["Qt"].ravel(), g["Qt"], rtol=1e-15)
+    np.testing.assert_allclose(r["Vt"].ravel(), g["Vt"], rtol=1e-14)
+    np.testing.assert_array_equal(r["I"].ravel(), g["I"].astype(int))
+    np.testing.assert_array_equal(r["E"].ravel(), g["E"].astype(int))
+    np.testing.assert_allclose(r["O"].ravel(), g["O"], rtol=1e-14)
+
+
+# ------------------------------------------------------ top-k and routing
+
+def _brute_topk(S, k):
+    """First k column indices of each row by (score desc, index asc), ascending."""
+    out = []
+    for row in S:
+        order = np.lexsort((np.arange(len(row)), -row))
+        out.append(np.sort(order[:k]))
+    return np.array(out)
+
+
+def _brute_route(R, s):
+    return np.array([np.lexsort((np.arange(len(r)), -r))[:s] for r in R])
+
+
+@pytest.mark.parametrize("N,d,m,k,s", [(200, 8, 5, 17, 2), (64, 4, 4, 64, 3), (50, 3, 10, 1, 1)])
+def test_topk_and_routes_match_brute_force(N, d, m, k, s):
+    rng = np.random.default_rng(5)
+    Q, K, V = (rng.standard_normal((2, N, d)) for _ in range(3))
+    r = oracle.forward(Q, K, V, m=m, k=k, s=s, threads=2)
+    for h in range(2):
+        Qt = Q[h].reshape(m, -1, d).mean(axis=1) if N % m == 0 else r["Qt"][h]
+        np.testing.assert_allclose(r["Qt"][h], Qt, rtol=1e-12, atol=1e-14)
+        np.testing.assert_array_equal(r["I"][h], _brute_topk(r["Qt"][h] @ K[h].T, k))
+        np.testing.assert_array_equal(r["E"][h], _brute_route(Q[h] @ r["Qt"][h].T, s))
+
+
+def test_topk_ties_go_to_lower_index():
+    # keys take 3 values only, so every score row is full of exact ties
+    rng = np.random.default_rng(7)
+    N, d, m, k = 120, 2, 4, 30
+    K = rng.integers(-1, 2, size=(1, N, d)).astype(np.float64)
+    Q = rng.integers(-1, 2, size=(1, N, d)).astype(np.float64)
+    V = rng.standard_normal((1, N, d))
+    r = oracle.forward(Q, K, V, m=m, k=k, s=2, threads=1)
+    S = r["Qt"][0] @ K[0].T
+    np.testing.assert_array_equal(r["I"][0], _brute_topk(S, k))
+    np.testing.assert_array_equal(r["E"][0], _brute_route(Q[0] @ r["Qt"][0].T, 2))
+
+
+def test_negative_zero_ties_with_zero():
+    # score rows of +0.0 and -0.0 are all equal: the lowest indices must win
+    N, d = 16, 1
+    K = np.zeros((1, N, d)); K[0, ::2, 0] = -0.0
+    Q = np.ones((1, N, d))
+    r = oracle.forward(Q, K, np.ones((1, N, d)), m=2, k=5, s=1, threads=1)
+    np.testing.assert_array_equal(r["I"][0], np.tile(np.arange(5), (2, 1)))
+
+
+# ------------------------------------------------ special-case identities
+
+def _sdpa(q, k, v, scale):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))[None]
+    return torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), scale=scale)[0].numpy()
+
+
+@pytest.mark.parametrize("scale", [0.0, 0.37])
+def test_no_shared_full_k_is_softmax_attention(scale):
+    N, d = 48, 6
+    Q, K, V = (_rand((1, N, d), i) for i in (10, 11, 12))
+    r = oracle.forward(Q, K, V, m=4, k=N, s=1, scale=scale, no_shared=True, threads=1)
+    tau = scale if scale > 0 else 1 / math.sqrt(d)
+    np.testing.assert_allclose(r["O"][0], _sdpa(Q[0], K[0], V[0], tau), rtol=1e-12, atol=1e-13)
+
+
+def test_shared_full_k_is_attention_over_landmarks_and_keys():
+    N, d, m = 40, 5, 8
+    Q, K, V = (_rand((1, N, d), i) for i in (20, 21, 22))
+    r = oracle.forward(Q, K, V, m=m, k=N, s=1, threads=1)
+    tau = 1 / math.sqrt(d)
+    Qt = torch.nn.functional.adaptive_avg_pool1d(torch.from_numpy(Q[0]).T[None], m)[0].T.numpy()
+    Vt = _sdpa(Qt, K[0], V[0], tau)
+    np.testing.assert_allclose(r["Vt"][0], Vt, rtol=1e-12, atol=1e-13)
+    ref = _sdpa(Q[0], np.concatenate([Qt, K[0]]), np.concatenate([Vt, V[0]]), tau)
+    np.testing.assert_allclose(r["O"][0], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_overlapping_experts_are_concatenated():
+    # all landmarks equal -> both experts hold every key -> each key is in two
+    # slots, i.e. its logit carries an extra ln 2 against the shared slots
+    N, d = 32, 4
+    q = _rand((1, 1, d), 30)
+    Q = np.repeat(q, N, axis=1)
+    K, V = _rand((1, N, d), 31), _rand((1, N, d), 32)
+    r = oracle.forward(Q, K, V, m=2, k=N, s=2, threads=1)
+    np.testing.assert_array_equal(r["E"][0], np.tile([0, 1], (N, 1)))
+    tau = 1 / math.sqrt(d)
+    keys = np.concatenate([r["Qt"][0], K[0]])
+    vals = np.concatenate([r["Vt"][0], V[0]])
+    logits = tau * q[0] @ keys.T
+    logits[:, 2:] += math.log(2.0)
+    w = np.exp(logits - logits.max())
+    ref = (w @ vals) / w.sum()
+    np.testing.assert_allclose(r["O"][0], np.repeat(ref, N, axis=0), rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------- invariants
+
+def test_joint_key_value_permutation():
+    N, d, m, k, s = 96, 6, 6, 11, 2
+    Q, K, V = (_rand((1, N, d), i) for i in (40, 41, 42))
+    perm = np.random.default_rng(43).permutation(N)
+    a = oracle.forward(Q, K, V, m=m, k=k, s=s, threads=1)
+    b = oracle.forward(Q, K[:, perm], V[:, perm], m=m, k=k, s=s, threads=1)
+    # key j of the permuted input is original key perm[j]
+    np.testing.assert_array_equal(np.sort(perm[b["I"][0]], axis=1), a["I"][0])
+    np.testing.assert_allclose(b["O"], a["O"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(b["Vt"], a["Vt"], rtol=1e-12, atol=1e-13)
+
+
+def test_outputs_in_convex_hull():
+    N, d, m, k, s = 128, 8, 8, 16, 3
+    Q, K, V = (_rand((1, N, d), i) for i in (50, 51, 52))
+    r = oracle.forward(Q, K, V, m=m, k=k, s=s, threads=1)
+    lo, hi = V[0].min(axis=0), V[0].max(axis=0)
+    assert np.all(r["Vt"][0] >= lo - 1e-12) and np.all(r["Vt"][0] <= hi + 1e-12)
+    vstar = np.concatenate([r["Vt"][0], V[0]])
+    assert np.all(r["O"][0] >= vstar.min(axis=0) - 1e-12)
+    assert np.all(r["O"][0] <= vstar.max(axis=0) + 1e-12)
+
+
+def test_operation_count_is_linear_in_N():
+    # multiply-adds: 2mNd (scores + Vt), Nmd (routing), 2N(m + sk)d (output)
+    for N, d, m, k, s in [(64, 4, 4, 8, 2), (256, 8, 16, 32, 3), (512, 2, 8, 5, 1)]:
+        Q, K, V = (_rand((1, N, d), i) for i in (60, 61, 62))
+        r = oracle.forward(Q, K, V, m=m, k=k, s=s, threads=1)
+        assert r["macs"] == 5 * N * m * d + 2 * N * s * k * d
+
+
+def test_query_subset_and_overrides_reproduce_full_run():
+    N, d, m, k, s = 80, 5, 5, 9, 2
+    Q, K, V = (_rand((2, N, d), i) for i in (70, 71, 72))
+    full = oracle.forward(Q, K, V, m=m, k=k, s=s, threads=2)
+    ids = np.array([3, 79, 0, 41])
+    sub = oracle.forward(Q, K, V, m=m, k=k, s=s, q_ids=ids, threads=2)
+    np.testing.assert_array_equal(sub["E"], full["E"][:, ids])
+    np.testing.assert_allclose(sub["O"], full["O"][:, ids], rtol=0, atol=0)
+    ov = oracle.forward(Q, K, V, m=m, k=k, s=s, I_override=full["I"], E_override=full["E"], threads=2)
+    np.testing.assert_allclose(ov["O"], full["O"], rtol=0, atol=0)
+    # a different, valid override changes the output exactly as a by-hand recomputation says
+    I2 = full["I"].copy(); I2[:, :, 0] = (I2[:, :, 0] + 1) % N
+    I2 = np.sort(I2, axis=2)
+    ov2 = oracle.forward(Q, K, V, m=m, k=k, s=s, q_ids=ids, I_override=I2, E_override=full["E"][:, ids],
+                         threads=2)
+    tau = 1 / math.sqrt(d)
+    for h in range(2):
+        for t, q in enumerate(ids):
+            keys = [full["Qt"][h]] + [K[h][I2[h, e]] for e in full["E"][h, q]]
+            vals = [full["Vt"][h]] + [V[h][I2[h, e]] for e in full["E"][h, q]]
+            lg = tau * np.concatenate(keys) @ Q[h, q]
+            w = np.exp(lg - lg.max())
+            np.testing.assert_allclose(ov2["O"][h, t], w @ np.concatenate(vals) / w.sum(), rtol=1e-12)
+
+
+def test_rejects_bad_parameters():
+    Q = np.zeros((1, 8, 2))
+    with pytest.raises(ValueError):
+        oracle.forward(Q, Q, Q, m=9, k=1, s=1)
+    with pytest.raises(ValueError):
+        oracle.forward(Q, Q, Q, m=2, k=9, s=1)
+    with pytest.raises(ValueError):
+        oracle.forward(Q, Q, Q, m=2, k=1, s=3)
