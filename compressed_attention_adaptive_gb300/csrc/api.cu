@@ -1,0 +1,293 @@
+// C ABI of libmita: argument validation, workspace carving and the order of
+// launches for each entry point (declared in include/mita.h).
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+
+#include "../../include/mita.h"
+#include "internal.h"
+
+namespace mita {
+
+static thread_local std::string g_last_error;
+
+static mita_status fail(mita_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+static mita_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(MITA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define MITA_CUDA(call, what)                              \
+    do {                                                   \
+        cudaError_t e_ = (call);                           \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+// Validates p and fills D. Returns MITA_OK or the error (with detail).
+static mita_status resolve(const mita_params* p, Dims* D) {
+    if (!p) return fail(MITA_ERR_INVALID_ARG, "params is NULL");
+    if (p->B < 1 || p->H < 1 || p->N < 1) return fail(MITA_ERR_INVALID_ARG, "B, H, N must be >= 1");
+    if (p->d < 8 || p->d > 256 || p->d % 8) return fail(MITA_ERR_INVALID_ARG, "d must be a multiple of 8 in [8, 256]");
+    if (p->m < 1 || p->m > p->N) return fail(MITA_ERR_INVALID_ARG, "m must be in [1, N]");
+    if (p->k < 1 || p->k > p->N) return fail(MITA_ERR_INVALID_ARG, "k must be in [1, N]");
+    if (p->s < 1 || p->s > p->m) return fail(MITA_ERR_INVALID_ARG, "s must be in [1, m]");
+    if (p->s > kMaxS) return fail(MITA_ERR_UNSUPPORTED, "s > %d is not supported", kMaxS);
+    if (p->dtype != MITA_DTYPE_F32 && p->dtype != MITA_DTYPE_BF16) return fail(MITA_ERR_INVALID_ARG, "bad dtype");
+    if (p->flags & ~(unsigned)(MITA_FLAG_NO_SHARED | MITA_FLAG_SIMT)) return fail(MITA_ERR_INVALID_ARG, "unknown flag");
+    if (!(p->scale >= 0.0f) || isinf(p->scale)) return fail(MITA_ERR_INVALID_ARG, "scale must be finite and >= 0");
+    if ((long long)p->B * p->H > 65535) return fail(MITA_ERR_UNSUPPORTED, "B*H must be <= 65535");
+    if ((long long)p->B * p->H * p->N >= (1LL << 31)) return fail(MITA_ERR_UNSUPPORTED, "B*H*N must be < 2^31");
+    D->B = p->B; D->H = p->H; D->BH = p->B * p->H; D->N = p->N; D->d = p->d;
+    D->m = p->m; D->k = p->k; D->s = p->s;
+    if (p->grid_h == 0) {
+        D->gh = 1; D->gw = p->N; D->lh = 1; D->lw = p->m;
+    } else {
+        if (p->grid_h < 1 || p->grid_w < 1 || (long long)p->grid_h * p->grid_w != p->N)
+            return fail(MITA_ERR_INVALID_ARG, "grid_h * grid_w must equal N");
+        if (p->lm_h < 1 || p->lm_w < 1 || p->lm_h * p->lm_w != p->m)
+            return fail(MITA_ERR_INVALID_ARG, "lm_h * lm_w must equal m");
+        if (p->lm_h > p->grid_h || p->lm_w > p->grid_w)
+            return fail(MITA_ERR_INVALID_ARG, "landmark grid larger than token grid");
+        D->gh = p->grid_h; D->gw = p->grid_w; D->lh = p->lm_h; D->lw = p->lm_w;
+    }
+    D->scale = p->scale > 0.0f ? p->scale : 1.0f / sqrtf((float)p->d);
+    D->flags = p->flags;
+    D->dtype = p->dtype;
+    D->shared = !(p->flags & MITA_FLAG_NO_SHARED);
+    if (out_simt_smem(*D) > 200 * 1024) return fail(MITA_ERR_UNSUPPORTED, "m + s*k too large for this build");
+    return MITA_OK;
+}
+
+static size_t elem_size(const Dims& D) { return D.dtype == MITA_DTYPE_F32 ? 4 : 2; }
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Sequential carving of one workspace allocation into 1 KiB-aligned buffers.
+struct Carver {
+    char* base;
+    size_t off = 0;
+    explicit Carver(void* b) : base((char*)b) {}
+    template <typename T> T* take(size_t count) {
+        off = align_up(off, 1024);
+        T* p = base ? (T*)(base + off) : nullptr;
+        off += count * sizeof(T);
+        return p;
+    }
+};
+
+static bool use_tc(const Dims& D) { return !(D.flags & MITA_FLAG_SIMT) && tc_supported(D); }
+
+struct Work {
+    int* status;
+    float* Qt;
+    float* Vt;
+    int32_t* I;
+    int32_t* E;
+    // CUDA-core path
+    float2* stats;
+    float* S;
+    float* R;
+    // tensor-core path
+    TcPlan plan;
+    TcWork tc;
+};
+
+static Work carve(const Dims& D, void* ws, size_t* bytes) {
+    Carver c(ws);
+    Work w{};
+    const size_t BH = D.BH;
+    w.status = c.take<int>(64);
+    w.Qt = c.take<float>(BH * D.m * D.d);
+    w.Vt = c.take<float>(BH * D.m * D.d);
+    w.I = c.take<int32_t>(BH * D.m * D.k);
+    w.E = c.take<int32_t>(BH * D.N * D.s);
+    if (!use_tc(D)) {
+        w.stats = c.take<float2>(BH * D.m);
+        w.S = c.take<float>(BH * D.m * D.N);
+        w.R = c.take<float>(BH * D.N * D.m);
+    } else {
+        const TcPlan P = tc_plan(D);
+        w.plan = P;
+        TcWork& t = w.tc;
+        t.Qhi = c.take<__nv_bfloat16>(BH * P.m_pad * D.d);
+        t.Qlo = c.take<__nv_bfloat16>(BH * P.m_pad * D.d);
+        t.Vtb = c.take<__nv_bfloat16>(BH * P.m_pad * D.d);
+        t.Opart = c.take<float>(BH * P.splits * P.m_pad * D.d);
+        t.ML = c.take<float2>(BH * P.splits * P.m_pad);
+        t.S = c.take<float>(BH * D.m * D.N);
+        t.counts = c.take<int>(BH * D.m * 2);
+        t.tile_ctr = c.take<int>(2);
+        t.zero_begin = t.counts;
+        t.zero_bytes = t.counts ? (size_t)((char*)(t.tile_ctr + 2) - (char*)t.counts) : 0;
+        t.cursors = c.take<int>(BH * D.m * 2);
+        t.toff = c.take<int>(BH * D.m);
+        t.tiles = c.take<int4>((size_t)P.max_tiles);
+        t.perm = c.take<int32_t>(BH * D.N * D.s);
+        t.part = c.take<__nv_bfloat16>(BH * D.N * D.s * D.d);
+        t.lse = c.take<float>(BH * D.N * D.s);
+        t.cnt = c.take<int>(BH * D.N);
+    }
+    *bytes = align_up(c.off, 1024);
+    return w;
+}
+
+static mita_status check_ws(const Dims& D, void* ws, size_t ws_bytes, Work* w) {
+    size_t need;
+    carve(D, nullptr, &need);
+    if (!ws) return fail(MITA_ERR_WORKSPACE, "workspace is NULL");
+    if ((uintptr_t)ws % 256) return fail(MITA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (ws_bytes < need) return fail(MITA_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+    *w = carve(D, ws, &need);
+    return MITA_OK;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+static mita_status run(const mita_params* p, const void* Q, const void* K, const void* V, void* O, float* Qt_out,
+                       int32_t* idx_out, int32_t* route_out, float* Vt_out, void* ws, size_t ws_bytes,
+                       void* stream, int upto) {
+    Dims D;
+    mita_status st = resolve(p, &D);
+    if (st) return st;
+    if (!Q || !aligned16(Q)) return fail(MITA_ERR_INVALID_ARG, "Q must be a 16-byte aligned device pointer");
+    if (upto >= 1 && (!K || !aligned16(K))) return fail(MITA_ERR_INVALID_ARG, "K must be a 16-byte aligned device pointer");
+    if (upto >= 2 && (!V || !aligned16(V))) return fail(MITA_ERR_INVALID_ARG, "V must be a 16-byte aligned device pointer");
+    if (upto >= 2 && (!O || !aligned16(O))) return fail(MITA_ERR_INVALID_ARG, "O must be a 16-byte aligned device pointer");
+    Work w;
+    st = check_ws(D, ws, ws_bytes, &w);
+    if (st) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    float* Qt = Qt_out ? Qt_out : w.Qt;
+    int32_t* I = idx_out ? idx_out : w.I;
+    int32_t* E = route_out ? route_out : w.E;
+    float* Vt = Vt_out ? Vt_out : w.Vt;
+
+    if (use_tc(D)) {
+        MITA_CUDA(launch_pool(D, Q, Qt, w.tc.Qhi, w.tc.Qlo, w.plan.m_pad, w.status, s), "landmark pooling");
+        if (upto == 0) return MITA_OK;
+        MITA_CUDA(launch_forward_tc(D, w.plan, w.tc, Q, K, V, O, Vt, I, (upto == 1 && !route_out) ? nullptr : E,
+                                    w.status, upto, s),
+                  "tensor-core forward");
+        return MITA_OK;
+    }
+    MITA_CUDA(launch_pool(D, Q, Qt, nullptr, nullptr, 0, w.status, s), "landmark pooling");
+    if (upto == 0) return MITA_OK;
+    MITA_CUDA(launch_select_simt(D, Q, K, Qt, w.S, w.R, I, (upto == 1 && !route_out) ? nullptr : E, s),
+              "expert selection");
+    if (upto == 1) return MITA_OK;
+    MITA_CUDA(launch_shared_simt(D, V, w.S, w.stats, Vt, s), "shared expert");
+    MITA_CUDA(launch_out_simt(D, Q, K, V, Qt, Vt, I, E, O, w.status, s), "expert attention");
+    return MITA_OK;
+}
+
+}  // namespace mita
+
+using namespace mita;
+
+extern "C" {
+
+size_t mita_workspace_size(const mita_params* p) {
+    Dims D;
+    if (resolve(p, &D)) return 0;
+    size_t bytes;
+    carve(D, nullptr, &bytes);
+    return bytes;
+}
+
+mita_status mita_landmarks(const mita_params* p, const void* Q, float* Qt, void* ws, size_t ws_bytes, void* stream) {
+    g_last_error.clear();
+    if (!Qt) return fail(MITA_ERR_INVALID_ARG, "Qt is NULL");
+    return run(p, Q, nullptr, nullptr, nullptr, Qt, nullptr, nullptr, nullptr, ws, ws_bytes, stream, 0);
+}
+
+mita_status mita_select(const mita_params* p, const void* Q, const void* K, int32_t* idx, int32_t* route, void* ws,
+                        size_t ws_bytes, void* stream) {
+    g_last_error.clear();
+    return run(p, Q, K, nullptr, nullptr, nullptr, idx, route, nullptr, ws, ws_bytes, stream, 1);
+}
+
+mita_status mita_forward(const mita_params* p, const void* Q, const void* K, const void* V, void* O,
+                         int32_t* idx_out, int32_t* route_out, float* Vt_out, void* ws, size_t ws_bytes,
+                         void* stream) {
+    g_last_error.clear();
+    return run(p, Q, K, V, O, nullptr, idx_out, route_out, Vt_out, ws, ws_bytes, stream, 2);
+}
+
+size_t mita_host_buffer_size(const mita_params* p) {
+    Dims D;
+    if (resolve(p, &D)) return 0;
+    const size_t t = align_up((size_t)D.BH * D.N * D.d * elem_size(D), 1024);
+    return 4 * t + mita_workspace_size(p);
+}
+
+mita_status mita_forward_host(const mita_params* p, const void* Q, const void* K, const void* V, void* O, void* dev,
+                              size_t dev_bytes, void* stream) {
+    g_last_error.clear();
+    Dims D;
+    mita_status st = resolve(p, &D);
+    if (st) return st;
+    if (!Q || !K || !V || !O) return fail(MITA_ERR_INVALID_ARG, "host buffers must not be NULL");
+    const size_t need = mita_host_buffer_size(p);
+    if (!dev || (uintptr_t)dev % 256) return fail(MITA_ERR_WORKSPACE, "device buffer NULL or not 256-byte aligned");
+    if (dev_bytes < need) return fail(MITA_ERR_WORKSPACE, "device buffer too small: %zu < %zu bytes", dev_bytes, need);
+    const size_t bytes = (size_t)D.BH * D.N * D.d * elem_size(D);
+    const size_t t = align_up(bytes, 1024);
+    char* b = (char*)dev;
+    cudaStream_t s = (cudaStream_t)stream;
+    MITA_CUDA(cudaMemcpyAsync(b, Q, bytes, cudaMemcpyHostToDevice, s), "copy Q to device");
+    MITA_CUDA(cudaMemcpyAsync(b + t, K, bytes, cudaMemcpyHostToDevice, s), "copy K to device");
+    MITA_CUDA(cudaMemcpyAsync(b + 2 * t, V, bytes, cudaMemcpyHostToDevice, s), "copy V to device");
+    st = run(p, b, b + t, b + 2 * t, b + 3 * t, nullptr, nullptr, nullptr, nullptr, b + 4 * t, dev_bytes - 4 * t,
+             stream, 2);
+    if (st) return st;
+    MITA_CUDA(cudaMemcpyAsync(O, b + 3 * t, bytes, cudaMemcpyDeviceToHost, s), "copy O to host");
+    return MITA_OK;
+}
+
+mita_status mita_device_status(void* ws, void* stream) {
+    g_last_error.clear();
+    if (!ws) return fail(MITA_ERR_WORKSPACE, "workspace is NULL");
+    cudaStream_t s = (cudaStream_t)stream;
+    MITA_CUDA(cudaStreamSynchronize(s), "stream synchronize");
+    int v = 0;
+    MITA_CUDA(cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost), "read device status");
+    const int zero = 0;
+    MITA_CUDA(cudaMemcpy(ws, &zero, sizeof zero, cudaMemcpyHostToDevice), "clear device status");
+    if (v == kStTimeout) return fail(MITA_ERR_TIMEOUT, "a bounded device wait ran out");
+    if (v == kStBounds) return fail(MITA_ERR_BOUNDS, "a device index was out of range");
+    if (v != 0) return fail(MITA_ERR_CUDA, "unexpected device status %d", v);
+    return MITA_OK;
+}
+
+const char* mita_status_string(mita_status s) {
+    switch (s) {
+        case MITA_OK: return "ok";
+        case MITA_ERR_INVALID_ARG: return "invalid argument";
+        case MITA_ERR_UNSUPPORTED: return "unsupported parameters";
+        case MITA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MITA_ERR_CUDA: return "CUDA error";
+        case MITA_ERR_TIMEOUT: return "device wait timed out";
+        case MITA_ERR_BOUNDS: return "device index out of range";
+    }
+    return "unknown status";
+}
+
+const char* mita_last_error(void) { return g_last_error.c_str(); }
+
+int mita_uses_tensor_cores(const mita_params* p) {
+    Dims D;
+    if (resolve(p, &D)) return -1;
+    return use_tc(D) ? 1 : 0;
+}
+
+}  // extern "C"

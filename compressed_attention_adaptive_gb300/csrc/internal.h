@@ -1,0 +1,68 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace mita {
+
+constexpr int kMaxS = 8;  // routed experts per query the kernels support
+
+// simt.cu
+cudaError_t launch_pool(const Dims& D, const void* Q, float* Qt, __nv_bfloat16* hi, __nv_bfloat16* lo, int m_pad,
+                        int* status, cudaStream_t st);
+cudaError_t launch_select_simt(const Dims& D, const void* Q, const void* K, const float* Qt, float* S, float* R,
+                               int32_t* I, int32_t* E, cudaStream_t st);
+cudaError_t launch_shared_simt(const Dims& D, const void* V, const float* S, float2* stats, float* Vt,
+                               cudaStream_t st);
+size_t out_simt_smem(const Dims& D);
+cudaError_t launch_out_simt(const Dims& D, const void* Q, const void* K, const void* V, const float* Qt,
+                            const float* Vt, const int32_t* I, const int32_t* E, void* O, int* status,
+                            cudaStream_t st);
+
+// select.cu
+cudaError_t launch_topk_dense(const float* S, long long rows, int N, int k, int32_t* I, cudaStream_t st);
+
+}  // namespace mita
+
+namespace mita {
+
+// tc.cu: sizes of the tensor-core path for one problem.
+struct TcPlan {
+    int m_pad;             // landmarks rounded up to 128
+    int m_tiles;           // m_pad / 128
+    int splits;            // key splits of the landmark pass
+    int chunks_per_split;  // 128-key chunks per split
+    long long max_tiles;   // upper bound on expert work tiles
+    int route_cols;        // TMEM columns of the routing kernel
+};
+
+// Workspace buffers of the tensor-core path.
+struct TcWork {
+    __nv_bfloat16 *Qhi, *Qlo, *Vtb;  // [BH][m_pad][d]
+    float* Opart;                    // [BH][splits][m_pad][d]
+    float2* ML;                      // [BH][splits][m_pad]
+    float* S;                        // [BH][m][N] raw landmark scores
+    int* counts;                     // [BH][m][2]
+    int* tile_ctr;                   // [2]: tiles written, tiles taken
+    void* zero_begin;                // counts .. tile_ctr, cleared each call
+    size_t zero_bytes;
+    int* cursors;                    // [BH][m][2]
+    int* toff;                       // [BH][m]
+    int4* tiles;                     // [max_tiles]
+    int32_t* perm;                   // [BH][N*s]
+    __nv_bfloat16* part;             // [BH][N][s][d]
+    float* lse;                      // [BH][N][s]
+    int* cnt;                        // [BH][N]
+};
+
+bool tc_supported(const Dims& D);
+TcPlan tc_plan(const Dims& D);
+cudaError_t launch_forward_tc(const Dims& D, const TcPlan& P, const TcWork& W, const void* Q, const void* K,
+                              const void* V, void* O, float* Vt, int32_t* I, int32_t* E, int* status, int upto,
+                              cudaStream_t st);
+
+}  // namespace mita

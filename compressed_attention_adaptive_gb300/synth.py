@@ -125,13 +125,16 @@ def _rng(seed, w: Workload, b, h, tensor):
     return np.random.default_rng(np.random.SeedSequence([seed, w.wid, b, h, _TENSORS[tensor]]))
 
 
-def _grf_kernel_hat(n, length_scale):
+def _grf_kernel_hat(gh, gw, length_scale):
     """Spectrum of a periodic Gaussian kernel whose white-noise convolution has
     covariance length-scale ``length_scale``, normalized to unit variance."""
     sigma = length_scale / math.sqrt(2.0)
-    r = np.minimum(np.arange(n), n - np.arange(n)).astype(np.float64)
-    g1 = np.exp(-(r ** 2) / (2 * sigma ** 2))
-    g = np.outer(g1, g1)
+
+    def g1(n):
+        r = np.minimum(np.arange(n), n - np.arange(n)).astype(np.float64)
+        return np.exp(-(r ** 2) / (2 * sigma ** 2))
+
+    g = np.outer(g1(gh), g1(gw))
     g /= math.sqrt((g ** 2).sum())
     return _fft.rfft2(g)
 
@@ -143,8 +146,7 @@ def _head(w: Workload, seed: int, b: int, h: int):
         return tuple(_rng(seed, w, b, h, t).standard_normal((N, d), dtype=np.float32) for t in "QKV")
     if w.kind == "grf2d":
         gh, gw = w.grid
-        assert gh == gw, "grf2d expects a square grid"
-        khat = _grf_kernel_hat(gh, w.length_scale)
+        khat = _grf_kernel_hat(gh, gw, w.length_scale)
         out = []
         for t in "QKV":
             rng = _rng(seed, w, b, h, t)

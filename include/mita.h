@@ -1,0 +1,134 @@
+/*
+ * mita.h -- C ABI of libmita.so, the GB300 (sm_103a) MiTA attention forward.
+ *
+ * The operation is the forward pass of "MiTA Attention: Efficient Fast-Weight
+ * Scaling via a Mixture of Top-k Activations" as summarized on gist.science:
+ *
+ *   landmarks    Qt = adaptive average pooling of Q, m rows      (Arabic ed. s2, "mechanism details";
+ *                                                                  Dutch ed. "Kernconcepten" 1)
+ *   shared       Vt = softmax(scale * Qt K^T) V                  (Arabic ed. s2: Vt = Atten(Qt, K, V))
+ *   expert sets  I_i = indices of the k largest k_j . qt_i       (Arabic ed. s2; Dutch ed. "Kernconcepten" 3)
+ *   routing      e_1(q) .. e_s(q)                                (Dutch ed. "Wiskundige Formulering")
+ *   output       O_q = softmax attention of q over
+ *                K* = [Qt, K_(e1), .., K_(es)], V* = [Vt, V_(e1), .., V_(es)]
+ *                                                                (Dutch ed. "Wiskundige Formulering")
+ *
+ * The summaries leave four points open; this library fixes them as follows:
+ *   - the shared expert's keys are Qt (its values are Vt);
+ *   - a query is routed to the s landmarks with the largest q . qt_i, ties to
+ *     the lower landmark index, listed by descending score;
+ *   - top-k ranks raw (unscaled) scores, ties to the lower key index, and each
+ *     I_i is returned in ascending key order;
+ *   - expert sets that overlap are concatenated (a key picked by two routed
+ *     experts fills two slots), and one softmax runs over all m + s*k slots.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are DEVICE pointers, contiguous, row-major [B, H, rows, d]
+ *     (d fastest). Q, K, V, O use `dtype`; Qt / Vt outputs are float32;
+ *     index outputs are int32.
+ *   - The caller owns all memory, including the workspace (device memory of at
+ *     least mita_workspace_size() bytes, 256-byte aligned). The library never
+ *     allocates, frees or synchronizes inside these calls.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream). Outputs are valid once the stream reaches them.
+ *   - Argument errors are returned synchronously before anything is enqueued.
+ *     A failed launch returns MITA_ERR_CUDA. Errors detected on the device
+ *     (an index out of range, a bounded wait that ran out) are written to a
+ *     status word inside the workspace and read with mita_device_status().
+ *   - Calls are reentrant; concurrent calls must use distinct workspaces.
+ */
+#ifndef MITA_H
+#define MITA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MITA_OK = 0,
+    MITA_ERR_INVALID_ARG = 1, /* bad shape, pointer, flag or dtype             */
+    MITA_ERR_UNSUPPORTED = 2, /* valid MiTA parameters this build cannot run   */
+    MITA_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or too small       */
+    MITA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed          */
+    MITA_ERR_TIMEOUT = 5,     /* device: a bounded wait gave up                */
+    MITA_ERR_BOUNDS = 6       /* device: an index was out of range             */
+} mita_status;
+
+typedef enum { MITA_DTYPE_F32 = 0, MITA_DTYPE_BF16 = 1 } mita_dtype;
+
+enum {
+    /* Leave the m shared slots out of the output softmax (only the routed
+     * experts remain). With k = N and s = 1 the output is plain softmax
+     * attention, which tests use as an identity. */
+    MITA_FLAG_NO_SHARED = 1u << 0,
+    /* Run every step on CUDA cores in fp32 even where the tensor-core path
+     * applies (a second GPU implementation for cross-checks). */
+    MITA_FLAG_SIMT = 1u << 1
+};
+
+typedef struct {
+    int B, H, N, d;   /* batch, heads, tokens, head dim (8 <= d <= 256, d % 8 == 0) */
+    int m, k, s;      /* landmarks (1..N), top-k width (1..N), routed experts (1..min(m, 8)) */
+    int grid_h, grid_w; /* token grid for 2-D pooling (grid_h * grid_w == N);
+                           grid_h == 0 means 1-D pooling over N tokens           */
+    int lm_h, lm_w;   /* landmark grid (lm_h * lm_w == m); ignored for 1-D      */
+    float scale;      /* softmax scale; 0 means 1/sqrt(d)                        */
+    unsigned flags;   /* MITA_FLAG_*                                             */
+    int dtype;        /* mita_dtype of Q, K, V and O                             */
+} mita_params;
+
+/* Bytes of device workspace needed for `p`; 0 if `p` is invalid. */
+size_t mita_workspace_size(const mita_params* p);
+
+/* Landmark queries only. Qt: float32 [B, H, m, d], caller-owned device memory. */
+mita_status mita_landmarks(const mita_params* p, const void* Q, float* Qt, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* Landmarks, expert index sets and routes, without the attention outputs.
+ * idx: int32 [B, H, m, k], each row ascending; route: int32 [B, H, N, s],
+ * descending routing score. Either output may be NULL. */
+mita_status mita_select(const mita_params* p, const void* Q, const void* K, int32_t* idx, int32_t* route,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/* The whole forward pass. O: [B, H, N, d] in `dtype`. idx_out ([B, H, m, k]),
+ * route_out ([B, H, N, s]) and Vt_out (float32 [B, H, m, d]) are optional
+ * (NULL to skip) copies of the intermediate index sets, routes and shared
+ * expert values. */
+mita_status mita_forward(const mita_params* p, const void* Q, const void* K, const void* V, void* O,
+                         int32_t* idx_out, int32_t* route_out, float* Vt_out, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* Bytes of DEVICE memory mita_forward_host() needs: room for Q, K, V and O
+ * plus the workspace. */
+size_t mita_host_buffer_size(const mita_params* p);
+
+/* The forward pass on HOST buffers: Q, K, V, O are host pointers (pinned
+ * memory gives full copy speed), `dev` is caller-owned device memory of at
+ * least mita_host_buffer_size() bytes. Copies Q, K, V to the device, runs the
+ * forward pass, copies O back, all enqueued on `stream`; the call returns
+ * without waiting, so the host buffers must stay valid until the stream has
+ * passed the copies. */
+mita_status mita_forward_host(const mita_params* p, const void* Q, const void* K, const void* V, void* O,
+                              void* dev, size_t dev_bytes, void* stream);
+
+/* Synchronizes `stream`, returns the device status word of workspace `ws`
+ * (MITA_OK if no device-side error was recorded) and clears it. */
+mita_status mita_device_status(void* ws, void* stream);
+
+/* Static description of a status code. */
+const char* mita_status_string(mita_status s);
+
+/* Detail of the last error returned on the calling thread ("" if none). */
+const char* mita_last_error(void);
+
+/* 1 if `p` runs on the tcgen05 tensor-core path, 0 if on CUDA cores, -1 if invalid. */
+int mita_uses_tensor_cores(const mita_params* p);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MITA_H */
