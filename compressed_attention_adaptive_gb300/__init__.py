@@ -86,6 +86,12 @@ def lib():
         L.mita_last_error.argtypes = []
         L.mita_last_error.restype = ctypes.c_char_p
         L.mita_uses_tensor_cores.argtypes = [P]
+        L.mita_launch_count.argtypes = []
+        L.mita_launch_count.restype = ctypes.c_longlong
+        L.mita_profile_begin.argtypes = [ctypes.c_int]
+        L.mita_profile_begin.restype = ctypes.c_int
+        L.mita_profile_end.argtypes = [ctypes.c_char_p, sz, ctypes.POINTER(ctypes.c_double), ctypes.c_int]
+        L.mita_profile_end.restype = ctypes.c_int
         for f in ("mita_landmarks", "mita_select", "mita_forward", "mita_forward_host", "mita_device_status",
                   "mita_uses_tensor_cores"):
             getattr(L, f).restype = ctypes.c_int
@@ -119,6 +125,25 @@ def mita_host_buffer_size(p: Params) -> int:
 
 def mita_uses_tensor_cores(p: Params) -> int:
     return int(lib().mita_uses_tensor_cores(ctypes.byref(p.c())))
+
+
+def mita_launch_count() -> int:
+    return int(lib().mita_launch_count())
+
+
+def mita_profile_begin(max_marks: int):
+    _check(lib().mita_profile_begin(int(max_marks)))
+
+
+def mita_profile_end() -> dict:
+    """Per-phase milliseconds summed over the calls since mita_profile_begin."""
+    names = ctypes.create_string_buffer(4096)
+    ms = (ctypes.c_double * 64)()
+    n = lib().mita_profile_end(names, 4096, ms, 64)
+    if n < 0:
+        raise MitaError(4, "profile read failed")
+    keys = names.value.decode().split("\n")[:n]
+    return {k: ms[i] for i, k in enumerate(keys)}
 
 
 def workspace(p: Params, device="cuda"):

@@ -5,7 +5,10 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
+#include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/mita.h"
 #include "internal.h"
@@ -13,6 +16,25 @@
 namespace mita {
 
 static thread_local std::string g_last_error;
+
+// ---------------------------------------------------------------- profiling
+// While a profile is open, every prof_mark() records a CUDA event on the
+// launching stream; mita_profile_end() sums the time between consecutive
+// marks per phase name.
+static std::atomic<long long> g_launches{0};
+static std::mutex g_prof_mu;
+static bool g_prof_on = false;
+static std::vector<std::pair<std::string, cudaEvent_t>> g_prof_marks;
+static std::vector<cudaEvent_t> g_prof_pool;
+
+void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+void prof_mark(cudaStream_t st, const char* phase) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on || g_prof_marks.size() >= g_prof_pool.size()) return;
+    cudaEvent_t ev = g_prof_pool[g_prof_marks.size()];
+    if (cudaEventRecord(ev, st) == cudaSuccess) g_prof_marks.emplace_back(phase, ev);
+}
 
 static mita_status fail(mita_status st, const char* fmt, ...) {
     char buf[512];
@@ -124,7 +146,10 @@ static Work carve(const Dims& D, void* ws, size_t* bytes) {
         t.Vtb = c.take<__nv_bfloat16>(BH * P.m_pad * D.d);
         t.Opart = c.take<float>(BH * P.splits * P.m_pad * D.d);
         t.ML = c.take<float2>(BH * P.splits * P.m_pad);
-        t.S = c.take<float>(BH * D.m * D.N);
+        t.Ssamp = c.take<float>(BH * D.m * (size_t)P.n_samp);
+        t.thr = c.take<float>(BH * D.m);
+        t.cand = c.take<int2>(BH * P.m_pad * (size_t)P.splits * (size_t)P.cand_cap);
+        t.ccount = c.take<int>(BH * P.m_pad * (size_t)P.splits);
         t.counts = c.take<int>(BH * D.m * 2);
         t.tile_ctr = c.take<int>(2);
         t.zero_begin = t.counts;
@@ -172,21 +197,29 @@ static mita_status run(const mita_params* p, const void* Q, const void* K, const
     int32_t* E = route_out ? route_out : w.E;
     float* Vt = Vt_out ? Vt_out : w.Vt;
 
+    prof_mark(s, "pool");
     if (use_tc(D)) {
         MITA_CUDA(launch_pool(D, Q, Qt, w.tc.Qhi, w.tc.Qlo, w.plan.m_pad, w.status, s), "landmark pooling");
-        if (upto == 0) return MITA_OK;
-        MITA_CUDA(launch_forward_tc(D, w.plan, w.tc, Q, K, V, O, Vt, I, (upto == 1 && !route_out) ? nullptr : E,
-                                    w.status, upto, s),
-                  "tensor-core forward");
+        if (upto > 0)
+            MITA_CUDA(launch_forward_tc(D, w.plan, w.tc, Q, K, V, O, Vt, I, (upto == 1 && !route_out) ? nullptr : E,
+                                        w.status, upto, s),
+                      "tensor-core forward");
+        prof_mark(s, "");
         return MITA_OK;
     }
     MITA_CUDA(launch_pool(D, Q, Qt, nullptr, nullptr, 0, w.status, s), "landmark pooling");
-    if (upto == 0) return MITA_OK;
-    MITA_CUDA(launch_select_simt(D, Q, K, Qt, w.S, w.R, I, (upto == 1 && !route_out) ? nullptr : E, s),
-              "expert selection");
-    if (upto == 1) return MITA_OK;
-    MITA_CUDA(launch_shared_simt(D, V, w.S, w.stats, Vt, s), "shared expert");
-    MITA_CUDA(launch_out_simt(D, Q, K, V, Qt, Vt, I, E, O, w.status, s), "expert attention");
+    if (upto > 0) {
+        prof_mark(s, "select");
+        MITA_CUDA(launch_select_simt(D, Q, K, Qt, w.S, w.R, I, (upto == 1 && !route_out) ? nullptr : E, s),
+                  "expert selection");
+    }
+    if (upto > 1) {
+        prof_mark(s, "shared");
+        MITA_CUDA(launch_shared_simt(D, V, w.S, w.stats, Vt, s), "shared expert");
+        prof_mark(s, "output");
+        MITA_CUDA(launch_out_simt(D, Q, K, V, Qt, Vt, I, E, O, w.status, s), "expert attention");
+    }
+    prof_mark(s, "");
     return MITA_OK;
 }
 
@@ -283,6 +316,55 @@ const char* mita_status_string(mita_status s) {
 }
 
 const char* mita_last_error(void) { return g_last_error.c_str(); }
+
+long long mita_launch_count(void) { return g_launches.load(); }
+
+mita_status mita_profile_begin(int max_marks) {
+    g_last_error.clear();
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (g_prof_on) return fail(MITA_ERR_INVALID_ARG, "a profile is already open");
+    if (max_marks < 2) return fail(MITA_ERR_INVALID_ARG, "max_marks must be >= 2");
+    while ((int)g_prof_pool.size() < max_marks) {
+        cudaEvent_t ev;
+        MITA_CUDA(cudaEventCreate(&ev), "create profiling event");
+        g_prof_pool.push_back(ev);
+    }
+    g_prof_marks.clear();
+    g_prof_on = true;
+    return MITA_OK;
+}
+
+int mita_profile_end(char* names, size_t names_bytes, double* ms, int max_phases) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_on = false;
+    std::vector<std::string> order;
+    std::vector<double> sum;
+    if (!g_prof_marks.empty() && cudaEventSynchronize(g_prof_marks.back().second) != cudaSuccess) return -1;
+    for (size_t i = 0; i + 1 < g_prof_marks.size(); ++i) {
+        const std::string& nm = g_prof_marks[i].first;
+        if (nm.empty()) continue;  // end-of-call marker
+        float t = 0.0f;
+        if (cudaEventElapsedTime(&t, g_prof_marks[i].second, g_prof_marks[i + 1].second) != cudaSuccess) return -1;
+        size_t j = 0;
+        while (j < order.size() && order[j] != nm) ++j;
+        if (j == order.size()) { order.push_back(nm); sum.push_back(0.0); }
+        sum[j] += t;
+    }
+    g_prof_marks.clear();
+    std::string joined;
+    int n = 0;
+    for (size_t j = 0; j < order.size() && n < max_phases; ++j, ++n) {
+        if (ms) ms[n] = sum[j];
+        joined += order[j];
+        joined += '\n';
+    }
+    if (names && names_bytes) {
+        size_t c = joined.size() < names_bytes - 1 ? joined.size() : names_bytes - 1;
+        memcpy(names, joined.data(), c);
+        names[c] = 0;
+    }
+    return n;
+}
 
 int mita_uses_tensor_cores(const mita_params* p) {
     Dims D;

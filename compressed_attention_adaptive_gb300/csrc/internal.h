@@ -11,6 +11,11 @@ namespace mita {
 
 constexpr int kMaxS = 8;  // routed experts per query the kernels support
 
+// api.cu: phase markers (CUDA events while profiling is on) and the count of
+// kernels launched by this library.
+void prof_mark(cudaStream_t st, const char* phase);
+void count_launch(int n = 1);
+
 // simt.cu
 cudaError_t launch_pool(const Dims& D, const void* Q, float* Qt, __nv_bfloat16* hi, __nv_bfloat16* lo, int m_pad,
                         int* status, cudaStream_t st);
@@ -25,6 +30,10 @@ cudaError_t launch_out_simt(const Dims& D, const void* Q, const void* K, const v
 
 // select.cu
 cudaError_t launch_topk_dense(const float* S, long long rows, int N, int k, int32_t* I, cudaStream_t st);
+cudaError_t launch_sample_threshold(const float* Ssamp, long long rows, int n_samp, int k, float* thr,
+                                    cudaStream_t st);
+cudaError_t launch_topk_cand(const int2* cand, const int* ccount, int splits, long long cap, int BH, int m, int m_pad,
+                             int N, int k, int32_t* I, int* status, cudaStream_t st);
 
 }  // namespace mita
 
@@ -38,6 +47,9 @@ struct TcPlan {
     int chunks_per_split;  // 128-key chunks per split
     long long max_tiles;   // upper bound on expert work tiles
     int route_cols;        // TMEM columns of the routing kernel
+    int R;                 // top-k sample stride (every R-th key)
+    int n_samp;            // sampled keys per row (>= k)
+    long long cand_cap;    // candidate records per (row, split)
 };
 
 // Workspace buffers of the tensor-core path.
@@ -45,7 +57,10 @@ struct TcWork {
     __nv_bfloat16 *Qhi, *Qlo, *Vtb;  // [BH][m_pad][d]
     float* Opart;                    // [BH][splits][m_pad][d]
     float2* ML;                      // [BH][splits][m_pad]
-    float* S;                        // [BH][m][N] raw landmark scores
+    float* Ssamp;                    // [BH][m][n_samp] sample scores
+    float* thr;                      // [BH][m] candidate thresholds
+    int2* cand;                      // [BH][m_pad][splits][cand_cap] (score, key) records
+    int* ccount;                     // [BH][m_pad][splits]
     int* counts;                     // [BH][m][2]
     int* tile_ctr;                   // [2]: tiles written, tiles taken
     void* zero_begin;                // counts .. tile_ctr, cleared each call

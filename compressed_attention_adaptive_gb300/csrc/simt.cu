@@ -303,6 +303,7 @@ static cudaError_t pool_t(const Dims& D, const void* Q, float* Qt, __nv_bfloat16
                           int* status, cudaStream_t st) {
     dim3 grid(hi ? m_pad : D.m, D.BH);
     k_pool<T><<<grid, 256, 0, st>>>((const T*)Q, Qt, hi, lo, m_pad, D, status);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -321,6 +322,7 @@ static cudaError_t select_simt_t(const Dims& D, const void* Q, const void* K, co
         k_gemm_nt<float, T><<<grid, 256, 0, st>>>(Qt, (long long)D.m * D.d, (const T*)K, (long long)D.N * D.d, S,
                                                   (long long)D.m * D.N, D.m, D.N, D.d);
     }
+    count_launch();
     cudaError_t e = launch_topk_dense(S, (long long)D.BH * D.m, D.N, D.k, I, st);
     if (e != cudaSuccess) return e;
     // routing scores R = Q Qt^T, then the top-s routes per query
@@ -330,6 +332,7 @@ static cudaError_t select_simt_t(const Dims& D, const void* Q, const void* K, co
                                                   (long long)D.N * D.m, D.N, D.m, D.d);
         const long long nq = (long long)D.BH * D.N;
         k_route_dense<<<(unsigned)((nq + 255) / 256), 256, 0, st>>>(R, nq, D.m, D.s, E);
+        count_launch(2);
     }
     return cudaGetLastError();
 }
@@ -346,6 +349,7 @@ static cudaError_t shared_simt_t(const Dims& D, const void* V, const float* S, f
     k_row_softmax_stats<<<D.BH * D.m, 256, 0, st>>>(S, D.N, D.scale, stats);
     dim3 grid((D.d + 63) / 64, (D.m + 63) / 64, D.BH);
     k_pv_simt<T><<<grid, 256, 0, st>>>(S, stats, (const T*)V, Vt, D.m, D.N, D.d, D.scale);
+    count_launch(2);
     return cudaGetLastError();
 }
 
@@ -371,6 +375,7 @@ static cudaError_t out_simt_t(const Dims& D, const void* Q, const void* K, const
     }
     k_out_simt<T><<<(unsigned)((long long)D.BH * D.N), 128, smem, st>>>((const T*)Q, (const T*)K, (const T*)V, Qt,
                                                                          Vt, I, E, (T*)O, D, status);
+    count_launch();
     return cudaGetLastError();
 }
 

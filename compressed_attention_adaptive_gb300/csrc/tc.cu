@@ -66,13 +66,22 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t sP, uint32_t sV, 
     }
 }
 
+// Where the landmark pass sends the raw scores of a row that pass the
+// row's threshold: (score, key index) records appended at cand[n++].
+struct CandOut {
+    int2* cand;  // nullptr: no emission
+    float thr;
+    int j0;      // key index of column 0 of the chunk
+    int n;
+};
+
 // Online softmax of this thread's row of one chunk of scores held in TMEM.
 // nk keys are valid; sl = scale * log2(e). The reference max moves only when
 // the chunk max exceeds it by more than 8 (probabilities stay <= 2^8), and
-// then O (TMEM) is rescaled. Raw scores are copied to `raw` when given.
+// then O (TMEM) is rescaled. Raw scores >= co.thr are emitted when co.cand.
 template <int D>
 __device__ __forceinline__ void chunk_softmax(uint32_t tS, uint32_t tO, uint8_t* sP, int nk, bool row_ok, float sl,
-                                              bool first, float& mref, float& l, float* raw) {
+                                              bool first, float& mref, float& l, CandOut& co) {
     const int r = threadIdx.x;
     float mx = -INFINITY;
 #pragma unroll 1
@@ -80,14 +89,10 @@ __device__ __forceinline__ void chunk_softmax(uint32_t tS, uint32_t tO, uint8_t*
         float v[32];
         tmem_ld32(tS + c0, v);
         tmem_wait_ld();
-        if (raw && row_ok) {
-            if (c0 + 32 <= nk && ((uintptr_t)raw & 15) == 0) {
+        if (co.cand && row_ok) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4*>(raw + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-            } else {
-                for (int j = 0; j < 32 && c0 + j < nk; ++j) raw[c0 + j] = v[j];
-            }
+            for (int j = 0; j < 32; ++j)
+                if (c0 + j < nk && v[j] >= co.thr) co.cand[co.n++] = make_int2(__float_as_int(v[j]), co.j0 + c0 + j);
         }
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -134,16 +139,39 @@ __device__ __forceinline__ void chunk_softmax(uint32_t tS, uint32_t tO, uint8_t*
     }
 }
 
-// Copies one 128-row operand tile: row t comes from src_row(t) (nullptr ->
-// zero row), D bf16 per row, into the swizzled layout at sbase.
+// Copies an R-row operand tile (R a multiple of 8): row t comes from
+// src_row(t) (nullptr -> zero row), D bf16 per row, into the swizzled layout
+// at sbase. src_row(-1) must return any valid global address.
 template <int D, typename RowPtr>
-__device__ __forceinline__ void load_tile(uint32_t sbase, RowPtr src_row) {
+__device__ __forceinline__ void load_rows(uint32_t sbase, int R, RowPtr src_row) {
     constexpr int CPR = D / 8;  // 16-byte chunks per row
 #pragma unroll 4
-    for (int i = threadIdx.x; i < kT * CPR; i += blockDim.x) {
+    for (int i = threadIdx.x; i < R * CPR; i += blockDim.x) {
         const int row = i / CPR, c = i % CPR;
         const __nv_bfloat16* p = src_row(row);
-        cp_async16(sbase + sw_off(row, c, kT), p ? (const void*)(p + c * 8) : (const void*)src_row(-1), p != nullptr);
+        cp_async16(sbase + sw_off(row, c, R), p ? (const void*)(p + c * 8) : (const void*)src_row(-1), p != nullptr);
+    }
+}
+
+template <int D, typename RowPtr>
+__device__ __forceinline__ void load_tile(uint32_t sbase, RowPtr src_row) {
+    load_rows<D>(sbase, kT, src_row);
+}
+
+// Keeps the SMAX largest keys seen so far, descending; a key equal to one
+// already held stays behind it, so with increasing indices ties go to the
+// lower index.
+template <int SMAX>
+__device__ __forceinline__ void top_insert(uint32_t (&bu)[SMAX], int (&bi)[SMAX], uint32_t u, int i) {
+#pragma unroll
+    for (int t = 0; t < SMAX; ++t) {
+        const bool gt = u > bu[t];
+        const uint32_t tu = bu[t];
+        const int ti = bi[t];
+        bu[t] = gt ? u : tu;
+        bi[t] = gt ? i : ti;
+        u = gt ? tu : u;
+        i = gt ? ti : i;
     }
 }
 
@@ -151,13 +179,15 @@ __device__ __forceinline__ void load_tile(uint32_t sbase, RowPtr src_row) {
 
 // ------------------------------------------------------------------------
 // Landmark pass: per (landmark tile, key split, head). S = Qhi K^T + Qlo K^T
-// (the bf16 split of fp32 Qt keeps the ranking scores at fp32 accuracy),
-// raw scores to S_out, and an online-softmax partial of Vt over the split.
+// (the bf16 split of fp32 Qt keeps the ranking scores at fp32 accuracy);
+// every score at or above its row's threshold is recorded as a top-k
+// candidate, and an online-softmax partial of Vt over the split is written.
 template <int D>
 __global__ void __launch_bounds__(128, 1)
     k_landmark_tc(const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
                   const __nv_bfloat16* __restrict__ Qhi, const __nv_bfloat16* __restrict__ Qlo,
-                  float* __restrict__ S_out, float* __restrict__ Opart, float2* __restrict__ ML, int N, int m, int m_pad,
+                  const float* __restrict__ thr, int2* __restrict__ cand, int* __restrict__ ccount,
+                  float* __restrict__ Opart, float2* __restrict__ ML, int N, int m, int m_pad,
                   int splits, int chunks_per_split, float sl, int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar;
@@ -196,6 +226,11 @@ __global__ void __launch_bounds__(128, 1)
     float mref = -INFINITY, l = 0.0f;
     bool ok = true;
     int c = 0;
+    const size_t crow = ((size_t)bh * m_pad + row) * splits + sp;  // this row's record region of this split
+    CandOut co;
+    co.cand = row_ok ? cand + crow * (size_t)chunks_per_split * kT : nullptr;
+    co.thr = row_ok ? thr[(size_t)bh * m + row] : 0.0f;
+    co.n = 0;
     for (int j0 = j_begin; j0 < j_end; j0 += kT, ++c) {
         const int nk = min(kT, j_end - j0);
         load_tile<D>(smem_u32(sK), [&](int t) { return (t >= 0 && t < nk) ? Kb + (size_t)(j0 + t) * D : (t < 0 ? Kb : nullptr); });
@@ -210,8 +245,8 @@ __global__ void __launch_bounds__(128, 1)
             mma_commit(&bar);
         }
         if (!(ok = sync_on_mma(&bar, phase, status))) break;
-        chunk_softmax<D>(tS, tO, sK, nk, row_ok, sl, c == 0, mref, l,
-                         row_ok ? S_out + ((size_t)bh * m + row) * N + j0 : nullptr);
+        co.j0 = j0;
+        chunk_softmax<D>(tS, tO, sK, nk, row_ok, sl, c == 0, mref, l, co);
         fence_proxy_async();
         fence_before_sync();
         __syncthreads();
@@ -238,11 +273,77 @@ __global__ void __launch_bounds__(128, 1)
             }
         }
         ML[orow] = make_float2(mref, l);
+        ccount[crow] = co.n;
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     if (r < 32) tmem_dealloc(tmem, 256);
+}
+
+// Sample pass of the top-k selection: raw scores of each landmark row against
+// every R-th key (n_samp keys), same MMA sequence as the landmark pass.
+template <int D>
+__global__ void __launch_bounds__(128)
+    k_sample_tc(const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ Qhi,
+                const __nv_bfloat16* __restrict__ Qlo, float* __restrict__ Ssamp, int N, int m, int m_pad, int R,
+                int n_samp, int chunks_per_cta, int* __restrict__ status) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tmem_slot;
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    constexpr int TILE = kT * D * 2;
+    uint8_t* sHi = sm;
+    uint8_t* sLo = sm + TILE;
+    uint8_t* sK = sm + 2 * TILE;
+    const int mt = blockIdx.x, cg = blockIdx.y, bh = blockIdx.z, r = threadIdx.x;
+    if (r < 32) tmem_alloc(&tmem_slot, 128);
+    if (r == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t tS = lane_base(tmem);
+    uint32_t phase = 0;
+    const size_t qrow0 = (size_t)bh * m_pad + (size_t)mt * kT;
+    load_tile<D>(smem_u32(sHi), [&](int t) { return Qhi + (qrow0 + (t < 0 ? 0 : t)) * D; });
+    load_tile<D>(smem_u32(sLo), [&](int t) { return Qlo + (qrow0 + (t < 0 ? 0 : t)) * D; });
+    const __nv_bfloat16* Kb = K + (size_t)bh * N * D;
+    const int row = mt * kT + r;
+    for (int c = cg * chunks_per_cta; c < (cg + 1) * chunks_per_cta && c * kT < n_samp; ++c) {
+        const int t0 = c * kT, nk = min(kT, n_samp - t0);
+        load_tile<D>(smem_u32(sK), [&](int t) {
+            return (t >= 0 && t < nk) ? Kb + (size_t)(t0 + t) * R * D : (t < 0 ? Kb : nullptr);
+        });
+        cp_async_wait_all();
+        fence_proxy_async();
+        __syncthreads();
+        if (r == 0) {
+            fence_after_sync();
+            issue_qk<D>(tS, smem_u32(sHi), smem_u32(sK), false);
+            issue_qk<D>(tS, smem_u32(sLo), smem_u32(sK), true);
+            mma_commit(&bar);
+        }
+        if (!sync_on_mma(&bar, phase, status)) break;
+        float* dst = Ssamp + ((size_t)bh * m + (row < m ? row : 0)) * n_samp + t0;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kT; c0 += 32) {
+            float v[32];
+            tmem_ld32(tS + c0, v);
+            tmem_wait_ld();
+            if (row < m)
+                for (int j = 0; j < 32 && c0 + j < nk; ++j) dst[c0 + j] = v[j];
+        }
+        fence_before_sync();
+        __syncthreads();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (r < 32) tmem_dealloc(tmem, 128);
 }
 
 // Merges the per-split partials: Vt = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
@@ -272,14 +373,149 @@ __global__ void k_vt_combine(const float* __restrict__ Opart, const float2* __re
 }
 
 // ------------------------------------------------------------------------
-// Routing: R = Q Qhi^T + Q Qlo^T for a 128-query tile (landmarks in chunks of
-// 128 TMEM columns), then each thread keeps the s best of its row (ties to the
-// lower landmark index). Also clears the per-query merge counters.
-template <int D>
-__global__ void __launch_bounds__(128)
+// Routing: R = Q Qhi^T + Q Qlo^T (the bf16 split of fp32 Qt keeps routing
+// scores at fp32 accuracy), then each thread keeps the s best landmarks of
+// its query row (ties to the lower landmark index). Also clears the
+// per-query merge counters.
+
+template <int SMAX>
+__device__ __forceinline__ void route_epilogue(uint32_t tR, int m, int s, int q, bool q_ok, int32_t* __restrict__ Erow,
+                                               int* __restrict__ cnt_q) {
+    uint32_t bu[SMAX];
+    int bi[SMAX];
+#pragma unroll
+    for (int t = 0; t < SMAX; ++t) { bu[t] = 0u; bi[t] = -1; }
+#pragma unroll 1
+    for (int c0 = 0; c0 < m; c0 += 32) {
+        float v[32];
+        tmem_ld32(tR + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (c0 + j < m) top_insert<SMAX>(bu, bi, order_key(v[j]), c0 + j);
+    }
+    if (q_ok) {
+#pragma unroll
+        for (int t = 0; t < SMAX; ++t)
+            if (t < s) Erow[t] = bi[t];
+        *cnt_q = 0;
+    }
+}
+
+// Persistent variant for m_pad <= 256: each CTA walks a contiguous range of
+// 128-query tiles; Qt (hi, lo) of the current head stays in shared memory and
+// the next query tile is loaded and multiplied while this tile's routes are
+// picked (two TMEM accumulators).
+template <int D, int SMAX>
+__global__ void __launch_bounds__(128, 1)
     k_route_tc(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Qhi,
-               const __nv_bfloat16* __restrict__ Qlo, int N, int m, int m_pad, int s, uint32_t tmem_cols,
-               int32_t* __restrict__ E, int* __restrict__ cnt, int* __restrict__ status) {
+               const __nv_bfloat16* __restrict__ Qlo, int N, int m, int m_pad, int s, int tiles_per_head,
+               int total_tiles, uint32_t tmem_cols, int32_t* __restrict__ E, int* __restrict__ cnt,
+               int* __restrict__ status) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tmem_slot;
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int QT = m_pad * D * 2;
+    uint8_t* sHi = sm;
+    uint8_t* sLo = sm + QT;
+    uint8_t* sQb[2] = {sm + 2 * QT, sm + 2 * QT + kT * D * 2};
+    const int r = threadIdx.x;
+    const int per = (total_tiles + gridDim.x - 1) / gridDim.x;
+    const int t_begin = blockIdx.x * per, t_end = min(total_tiles, t_begin + per);
+    if (t_begin >= t_end) return;
+    if (r < 32) tmem_alloc(&tmem_slot, tmem_cols);
+    if (r == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    uint32_t phase = 0;
+    const uint32_t idR = idesc_bf16(128, m_pad, 0, 0);
+
+    auto load_q = [&](int t, int b) {
+        const int bh = t / tiles_per_head, q0 = (t % tiles_per_head) * kT;
+        const __nv_bfloat16* Qb = Q + (size_t)bh * N * D;
+        load_tile<D>(smem_u32(sQb[b]), [&](int i) {
+            return i < 0 ? Qb : (q0 + i < N ? Qb + (size_t)(q0 + i) * D : nullptr);
+        });
+    };
+    auto load_landmarks = [&](int bh) {
+        const __nv_bfloat16* h = Qhi + (size_t)bh * m_pad * D;
+        const __nv_bfloat16* lo = Qlo + (size_t)bh * m_pad * D;
+        load_rows<D>(smem_u32(sHi), m_pad, [&](int i) { return h + (size_t)(i < 0 ? 0 : i) * D; });
+        load_rows<D>(smem_u32(sLo), m_pad, [&](int i) { return lo + (size_t)(i < 0 ? 0 : i) * D; });
+    };
+    auto issue = [&](int b) {
+        const uint32_t tR = tmem + b * m_pad;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t offa = (kk >> 2) * kT * 128 + (kk & 3) * 32;
+            const uint32_t offb = (kk >> 2) * m_pad * 128 + (kk & 3) * 32;
+            mma_bf16(tR, sdesc(smem_u32(sQb[b]) + offa, 16, 1024), sdesc(smem_u32(sHi) + offb, 16, 1024), idR,
+                     kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t offa = (kk >> 2) * kT * 128 + (kk & 3) * 32;
+            const uint32_t offb = (kk >> 2) * m_pad * 128 + (kk & 3) * 32;
+            mma_bf16(tR, sdesc(smem_u32(sQb[b]) + offa, 16, 1024), sdesc(smem_u32(sLo) + offb, 16, 1024), idR, 1u);
+        }
+        mma_commit(&bar);
+    };
+
+    int t = t_begin, b = 0;
+    load_landmarks(t / tiles_per_head);
+    load_q(t, 0);
+    cp_async_wait_all();
+    fence_proxy_async();
+    __syncthreads();
+    if (r == 0) {
+        fence_after_sync();
+        issue(0);
+    }
+    for (; t < t_end; ++t, b ^= 1) {
+        const int tn = t + 1;
+        const bool has_next = tn < t_end;
+        const bool new_head = has_next && (tn / tiles_per_head != t / tiles_per_head);
+        if (has_next && !new_head) load_q(tn, b ^ 1);
+        if (!sync_on_mma(&bar, phase, status)) break;  // MMA(t) done: its Q tile and the landmarks are free
+        if (has_next) {
+            if (new_head) {
+                load_landmarks(tn / tiles_per_head);
+                load_q(tn, b ^ 1);
+            }
+            cp_async_wait_all();
+            fence_proxy_async();
+            __syncthreads();
+            if (r == 0) {
+                fence_after_sync();
+                issue(b ^ 1);
+            }
+        }
+        const int bh = t / tiles_per_head, q = (t % tiles_per_head) * kT + r;
+        const bool q_ok = q < N;
+        route_epilogue<SMAX>(lane_base(tmem) + b * m_pad, m, s, q, q_ok, E + ((size_t)bh * N + (q_ok ? q : 0)) * s,
+                             cnt + (size_t)bh * N + (q_ok ? q : 0));
+        fence_before_sync();
+    }
+    // drain an MMA still in flight if the loop left early
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (r < 32) tmem_dealloc(tmem, tmem_cols);
+}
+
+// Variant for m_pad > 256: one CTA per 128-query tile, landmarks streamed in
+// 128-row chunks into consecutive TMEM column blocks.
+template <int D, int SMAX>
+__global__ void __launch_bounds__(128)
+    k_route_chunked_tc(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Qhi,
+                       const __nv_bfloat16* __restrict__ Qlo, int N, int m, int m_pad, int s, uint32_t tmem_cols,
+                       int32_t* __restrict__ E, int* __restrict__ cnt, int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar;
     __shared__ uint32_t tmem_slot;
@@ -320,31 +556,10 @@ __global__ void __launch_bounds__(128)
         if (!(ok = sync_on_mma(&bar, phase, status))) break;
     }
     if (ok) {
-        uint32_t bu[kMaxS];
-        int bi[kMaxS];
-        for (int t = 0; t < s; ++t) { bu[t] = 0u; bi[t] = -1; }
-        for (int c0 = 0; c0 < m; c0 += 32) {
-            float v[32];
-            tmem_ld32(tR + c0, v);
-            tmem_wait_ld();
-            for (int j = 0; j < 32 && c0 + j < m; ++j) {
-                const uint32_t u = order_key(v[j]);
-                if (bi[s - 1] >= 0 && u <= bu[s - 1]) continue;
-                int pos = s - 1;
-                while (pos > 0 && (bi[pos - 1] < 0 || u > bu[pos - 1])) {
-                    bu[pos] = bu[pos - 1];
-                    bi[pos] = bi[pos - 1];
-                    --pos;
-                }
-                bu[pos] = u;
-                bi[pos] = c0 + j;
-            }
-        }
         const int q = q0 + r;
-        if (q < N) {
-            for (int t = 0; t < s; ++t) E[((size_t)bh * N + q) * s + t] = bi[t];
-            cnt[(size_t)bh * N + q] = 0;
-        }
+        const bool q_ok = q < N;
+        route_epilogue<SMAX>(tR, m, s, q, q_ok, E + ((size_t)bh * N + (q_ok ? q : 0)) * s,
+                             cnt + (size_t)bh * N + (q_ok ? q : 0));
     }
     fence_before_sync();
     __syncthreads();
@@ -544,7 +759,9 @@ __global__ void __launch_bounds__(128)
             }
             if (!(ok = sync_on_mma(&bar, phase, status))) break;
             const bool row_ok = q >= 0 && (!shc || r < shrows);
-            chunk_softmax<D>(tS, tO, sK, nk, row_ok, sl, c == 0, mref, l, nullptr);
+            CandOut none;
+            none.cand = nullptr;
+            chunk_softmax<D>(tS, tO, sK, nk, row_ok, sl, c == 0, mref, l, none);
             fence_proxy_async();
             fence_before_sync();
             __syncthreads();
@@ -646,16 +863,62 @@ TcPlan tc_plan(const Dims& D) {
     p.splits = (nchunks + p.chunks_per_split - 1) / p.chunks_per_split;
     p.max_tiles = (long long)D.BH * ((long long)D.N * D.s / kT + D.m + 1);
     int cols = 32;
-    while (cols < p.m_pad) cols <<= 1;
+    const int want = p.m_pad <= 256 ? 2 * p.m_pad : p.m_pad;
+    while (cols < want) cols <<= 1;
     p.route_cols = cols;
+    // sample stride ~ sqrt(N / 2k) balances the sample pass against the
+    // candidates it lets through (about R * k per row); n_samp >= k always
+    int R = (int)sqrt((double)D.N / (2.0 * D.k));
+    if (R > D.N / D.k) R = D.N / D.k;
+    if (R > 32) R = 32;
+    if (R < 1) R = 1;
+    p.R = R;
+    p.n_samp = (D.N + R - 1) / R;
+    p.cand_cap = (long long)p.chunks_per_split * kT;
     return p;
 }
 
-bool tc_supported(const Dims& D) { return D.dtype == 1 && (D.d == 64 || D.d == 128) && D.m <= 512; }
+bool tc_supported(const Dims& D) {
+    return D.dtype == 1 && (D.d == 64 || D.d == 128) && D.m <= 512 && D.N <= (1 << 20);
+}
 
 template <typename F>
 static cudaError_t set_smem(F* f, int bytes) {
     return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int DD, int SMAX>
+static cudaError_t launch_route_s(const Dims& D, const TcPlan& P, const TcWork& W, const __nv_bfloat16* q,
+                                  int32_t* E, int* status, cudaStream_t st) {
+    cudaError_t e;
+    const int tile = kT * DD * 2;
+    if (P.m_pad <= 256) {
+        const int smem = 2 * P.m_pad * DD * 2 + 2 * tile + 1024;
+        if ((e = set_smem(k_route_tc<DD, SMAX>, smem))) return e;
+        const int tph = (D.N + kT - 1) / kT;
+        const int total = tph * D.BH;
+        const int grid = std::min(total, num_sms());
+        k_route_tc<DD, SMAX><<<grid, 128, smem, st>>>(q, W.Qhi, W.Qlo, D.N, D.m, P.m_pad, D.s, tph, total,
+                                                      (uint32_t)P.route_cols, E, W.cnt, status);
+    } else {
+        const int smem = std::max(3 * tile, 100 * 1024) + 1024;
+        if ((e = set_smem(k_route_chunked_tc<DD, SMAX>, smem))) return e;
+        dim3 grid((D.N + kT - 1) / kT, D.BH);
+        k_route_chunked_tc<DD, SMAX><<<grid, 128, smem, st>>>(q, W.Qhi, W.Qlo, D.N, D.m, P.m_pad, D.s,
+                                                              (uint32_t)P.route_cols, E, W.cnt, status);
+    }
+    if ((e = cudaGetLastError())) return e;
+    count_launch();
+    return cudaSuccess;
+}
+
+template <int DD>
+static cudaError_t launch_route(const Dims& D, const TcPlan& P, const TcWork& W, const __nv_bfloat16* q, int32_t* E,
+                                int* status, cudaStream_t st) {
+    if (D.s <= 1) return launch_route_s<DD, 1>(D, P, W, q, E, status, st);
+    if (D.s <= 2) return launch_route_s<DD, 2>(D, P, W, q, E, status, st);
+    if (D.s <= 4) return launch_route_s<DD, 4>(D, P, W, q, E, status, st);
+    return launch_route_s<DD, 8>(D, P, W, q, E, status, st);
 }
 
 template <int DD>
@@ -668,32 +931,46 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
     const float sl = D.scale * 1.4426950408889634f;
     const int tile = kT * DD * 2;
     cudaError_t e;
-    // landmark pass: scores for the top-k and the shared-expert partials
+    // top-k threshold from a strided sample of the keys
+    prof_mark(st, "topk_sample");
+    {
+        const int smem = std::max(3 * tile, 100 * 1024) + 1024;
+        if ((e = set_smem(k_sample_tc<DD>, smem))) return e;
+        const int cpc = 4;
+        const int groups = (P.n_samp + cpc * kT - 1) / (cpc * kT);
+        k_sample_tc<DD><<<dim3(P.m_tiles, groups, D.BH), 128, smem, st>>>(kk, W.Qhi, W.Qlo, W.Ssamp, D.N, D.m,
+                                                                         P.m_pad, P.R, P.n_samp, cpc, status);
+        if ((e = cudaGetLastError())) return e;
+        count_launch();
+        if ((e = launch_sample_threshold(W.Ssamp, (long long)D.BH * D.m, P.n_samp, D.k, W.thr, st))) return e;
+    }
+    // landmark pass: top-k candidates and the shared-expert partials
+    prof_mark(st, "landmark");
     {
         const int smem = std::max(3 * tile + kp_bytes<DD>(), 100 * 1024) + 1024;
         if ((e = set_smem(k_landmark_tc<DD>, smem))) return e;
         dim3 grid(P.m_tiles, P.splits, D.BH);
-        k_landmark_tc<DD><<<grid, 128, smem, st>>>(kk, v, W.Qhi, W.Qlo, W.S, W.Opart, W.ML, D.N, D.m, P.m_pad,
-                                                  P.splits, P.chunks_per_split, sl, status);
+        k_landmark_tc<DD><<<grid, 128, smem, st>>>(kk, v, W.Qhi, W.Qlo, W.thr, W.cand, W.ccount, W.Opart, W.ML, D.N,
+                                                  D.m, P.m_pad, P.splits, P.chunks_per_split, sl, status);
         if ((e = cudaGetLastError())) return e;
+        count_launch();
     }
-    if ((e = launch_topk_dense(W.S, (long long)D.BH * D.m, D.N, D.k, I, st))) return e;
+    prof_mark(st, "topk_select");
+    if ((e = launch_topk_cand(W.cand, W.ccount, P.splits, P.cand_cap, D.BH, D.m, P.m_pad, D.N, D.k, I, status, st)))
+        return e;
     if (upto >= 2) {
+        prof_mark(st, "vt_combine");
+        count_launch();
         k_vt_combine<<<dim3(P.m_pad, D.BH), DD, 0, st>>>(W.Opart, W.ML, P.splits, D.m, P.m_pad, DD, Vt, W.Vtb);
         if ((e = cudaGetLastError())) return e;
     }
     if (!E) return cudaSuccess;
     // routing
-    {
-        const int smem = std::max(3 * tile, 100 * 1024) + 1024;
-        if ((e = set_smem(k_route_tc<DD>, smem))) return e;
-        dim3 grid((D.N + kT - 1) / kT, D.BH);
-        k_route_tc<DD><<<grid, 128, smem, st>>>(q, W.Qhi, W.Qlo, D.N, D.m, P.m_pad, D.s, (uint32_t)P.route_cols, E,
-                                               W.cnt, status);
-        if ((e = cudaGetLastError())) return e;
-    }
+    prof_mark(st, "route");
+    if ((e = launch_route<DD>(D, P, W, q, E, status, st))) return e;
     if (upto < 2) return cudaSuccess;
     // bucketing
+    prof_mark(st, "bucket");
     if ((e = cudaMemsetAsync(W.zero_begin, 0, W.zero_bytes, st))) return e;
     {
         const int use_smem = D.m <= 4096;
@@ -702,8 +979,10 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
         k_bucket_scan<<<D.BH, 512, 0, st>>>(W.counts, D.m, D.N * D.s, W.cursors, W.toff, W.tile_ctr, W.tiles);
         k_bucket_scatter<<<grid, 256, 0, st>>>(E, D.N, D.m, D.s, W.cursors, W.perm);
         if ((e = cudaGetLastError())) return e;
+        count_launch(3);
     }
     // expert attention + merge
+    prof_mark(st, "expert");
     {
         const int smem = std::max(2 * tile + kp_bytes<DD>(), 100 * 1024) + 1024;
         if ((e = set_smem(k_expert_tc<DD>, smem))) return e;
@@ -711,6 +990,7 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
                                                           W.tile_ctr + 1, (__nv_bfloat16*)O, W.part, W.lse, W.cnt,
                                                           D.N, D.m, P.m_pad, D.k, D.s, D.shared ? 1 : 0, sl, status);
         if ((e = cudaGetLastError())) return e;
+        count_launch();
     }
     return cudaSuccess;
 }

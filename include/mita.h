@@ -127,6 +127,23 @@ const char* mita_last_error(void);
 /* 1 if `p` runs on the tcgen05 tensor-core path, 0 if on CUDA cores, -1 if invalid. */
 int mita_uses_tensor_cores(const mita_params* p);
 
+/* ---- measurement hooks (not part of the method) ---------------------------
+ * Number of kernels this library has launched in the process so far. */
+long long mita_launch_count(void);
+
+/* Opens a phase profile: until mita_profile_end(), every call records a CUDA
+ * event on its stream at the start of each phase (landmark pooling, landmark
+ * pass, top-k selection, shared-expert combine, routing, bucketing, expert
+ * attention) and at its end; up to max_marks events in total (created here,
+ * kept for reuse). Process-wide; not for concurrent calls. */
+mita_status mita_profile_begin(int max_marks);
+
+/* Closes the profile: waits for the last event, sums the milliseconds of each
+ * phase over all profiled calls into ms[i] and writes the phase names,
+ * newline-separated, into `names`. Returns the number of phases (<= max_phases)
+ * or -1 on a CUDA error. */
+int mita_profile_end(char* names, size_t names_bytes, double* ms, int max_phases);
+
 #ifdef __cplusplus
 }
 #endif
