@@ -161,6 +161,11 @@ static Work carve(const Dims& D, void* ws, size_t* bytes) {
         t.part = c.take<__nv_bfloat16>(BH * D.N * D.s * D.d);
         t.lse = c.take<float>(BH * D.N * D.s);
         t.cnt = c.take<int>(BH * D.N);
+        if (P.resident) {
+            t.sh_part = c.take<__nv_bfloat16>(BH * D.N * D.d);
+            t.sh_lse = c.take<float>(BH * D.N);
+            t.Qp = c.take<__nv_bfloat16>(BH * D.N * D.s * D.d);
+        }
     }
     *bytes = align_up(c.off, 1024);
     return w;
@@ -318,6 +323,7 @@ const char* mita_status_string(mita_status s) {
 const char* mita_last_error(void) { return g_last_error.c_str(); }
 
 long long mita_launch_count(void) { return g_launches.load(); }
+
 
 mita_status mita_profile_begin(int max_marks) {
     g_last_error.clear();

@@ -50,6 +50,7 @@ struct TcPlan {
     int R;                 // top-k sample stride (every R-th key)
     int n_samp;            // sampled keys per row (>= k)
     long long cand_cap;    // candidate records per (row, split)
+    bool resident;         // expert keys resident in shared memory, shared slots in the routing pass
 };
 
 // Workspace buffers of the tensor-core path.
@@ -72,6 +73,9 @@ struct TcWork {
     __nv_bfloat16* part;             // [BH][N][s][d]
     float* lse;                      // [BH][N][s]
     int* cnt;                        // [BH][N]
+    __nv_bfloat16* sh_part;          // [BH][N][d] shared-slot partial (resident-key path)
+    float* sh_lse;                   // [BH][N]
+    __nv_bfloat16* Qp;               // [BH][N*s][d] queries in bucket order (resident-key path)
 };
 
 bool tc_supported(const Dims& D);

@@ -15,11 +15,25 @@
 // online softmax and writes its probabilities (bf16) into the swizzled P tile
 // that the second MMA (O += P V) reads. Thread 0 issues the MMAs; completion
 // is signalled through an mbarrier with a bounded wait.
+#include <cuda.h>
+
 #include "internal.h"
 #include "tc.cuh"
 
 namespace mita {
 using namespace tc;
+
+#ifdef MITA_TRACE
+// Each event is (SM clock << 8 | tag) in a per-role log of block 0.
+constexpr int kTraceCap = 16384;
+__device__ unsigned long long g_mita_trace[4 * kTraceCap];
+__device__ int g_mita_trace_n[4];
+__device__ __forceinline__ void trace_ev(int role, int tag) {
+    if (blockIdx.x != 0 || blockIdx.y != 0) return;
+    const int i = atomicAdd(&g_mita_trace_n[role], 1);
+    if (i < kTraceCap) g_mita_trace[role * kTraceCap + i] = ((unsigned long long)clock64() << 8) | (unsigned)tag;
+}
+#endif
 
 namespace {
 
@@ -74,6 +88,24 @@ struct CandOut {
     int j0;      // key index of column 0 of the chunk
     int n;
 };
+
+// Issues O (+)= P * V with P (128 x 128 bf16) in TMEM at column tP (eight
+// columns per 16 keys) and V an MN-major 128 keys x D tile in shared memory.
+template <int D>
+__device__ __forceinline__ void issue_pv_ts(uint32_t tO, uint32_t tP, uint32_t sV, bool accumulate) {
+    constexpr uint32_t id = idesc_bf16(128, D, 0, 1);
+#pragma unroll
+    for (int kk = 0; kk < kT / 16; ++kk)
+        mma_bf16_ts(tO, tP + kk * 8, sdesc(sV + kk * 2048, kT * 128, 1024), id, (kk > 0 || accumulate) ? 1u : 0u);
+}
+
+// This thread's 128 probabilities, bf16 packed two per column, into TMEM
+// columns tP .. tP + 63 of its lane (warp-collective).
+__device__ __forceinline__ void tmem_store_p(uint32_t tP, const uint32_t (&pk)[64]) {
+    tmem_st32(tP, reinterpret_cast<const float*>(pk));
+    tmem_st32(tP + 32, reinterpret_cast<const float*>(pk + 32));
+    tmem_wait_st();
+}
 
 // Online softmax of this thread's row of one chunk of scores held in TMEM.
 // nk keys are valid; sl = scale * log2(e). The reference max moves only when
@@ -509,6 +541,171 @@ __global__ void __launch_bounds__(128, 1)
     if (r < 32) tmem_dealloc(tmem, tmem_cols);
 }
 
+// Variant for m_pad == 128 that also computes each query's shared-slot
+// partial: the routing scores R = Q Qt^T are the shared slots' logits (scaled),
+// so the same row gives the routes and softmax(scale R) Vt, written as a
+// normalized bf16 partial output with its log2-sum-exp. Qt (hi, lo) and Vt of
+// the current head stay in shared memory; the probabilities overwrite the
+// row's scores in TMEM and feed the P Vt MMA from there.
+template <int D, int SMAX>
+__global__ void __launch_bounds__(128, 1)
+    k_route_shared_tc(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Qhi,
+                      const __nv_bfloat16* __restrict__ Qlo, const __nv_bfloat16* __restrict__ Vtb, int N, int m,
+                      int s, int tiles_per_head, int total_tiles, float sl, int32_t* __restrict__ E,
+                      int* __restrict__ cnt, __nv_bfloat16* __restrict__ sh_part, float* __restrict__ sh_lse,
+                      int* __restrict__ status) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t bar_r, bar_o;  // R MMAs / the P Vt MMA
+    __shared__ uint32_t tmem_slot;
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    constexpr int TILE = kT * D * 2;
+    uint8_t* sHi = sm;
+    uint8_t* sLo = sm + TILE;
+    uint8_t* sVt = sm + 2 * TILE;
+    uint8_t* sQb[2] = {sm + 3 * TILE, sm + 4 * TILE};
+    constexpr uint32_t kO = 256;  // TMEM: R buffers at columns 0 / 128, the shared output at 256
+    const int r = threadIdx.x;
+    const int per = (total_tiles + gridDim.x - 1) / gridDim.x;
+    const int t_begin = blockIdx.x * per, t_end = min(total_tiles, t_begin + per);
+    if (t_begin >= t_end) return;
+    if (r < 32) tmem_alloc(&tmem_slot, 512);
+    if (r == 0) {
+        mbar_init(&bar_r, 1);
+        mbar_init(&bar_o, 1);
+        fence_mbar_init();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    uint32_t phase_r = 0, phase_o = 0;
+
+    auto load_q = [&](int t, int b) {
+        const int bh = t / tiles_per_head, q0 = (t % tiles_per_head) * kT;
+        const __nv_bfloat16* Qb = Q + (size_t)bh * N * D;
+        load_tile<D>(smem_u32(sQb[b]), [&](int i) {
+            return i < 0 ? Qb : (q0 + i < N ? Qb + (size_t)(q0 + i) * D : nullptr);
+        });
+    };
+    auto load_landmarks = [&](int bh) {
+        const size_t base = (size_t)bh * kT;
+        load_tile<D>(smem_u32(sHi), [&](int i) { return Qhi + (base + (i < 0 ? 0 : i)) * D; });
+        load_tile<D>(smem_u32(sLo), [&](int i) { return Qlo + (base + (i < 0 ? 0 : i)) * D; });
+        load_tile<D>(smem_u32(sVt), [&](int i) { return Vtb + (base + (i < 0 ? 0 : i)) * D; });
+    };
+    auto ready = [&]() {  // this thread's copies landed and are visible to the MMA
+        cp_async_wait_all();
+        fence_proxy_async();
+        __syncthreads();
+    };
+    auto issue_r = [&](int b) {
+        if (r == 0) {
+            fence_after_sync();
+            issue_qk<D>(tmem + b * kT, smem_u32(sQb[b]), smem_u32(sHi), false);
+            issue_qk<D>(tmem + b * kT, smem_u32(sQb[b]), smem_u32(sLo), true);
+            mma_commit(&bar_r);
+        }
+    };
+
+    auto head = [&](int t) { return t / tiles_per_head; };
+    int t = t_begin, b = 0;
+    load_landmarks(head(t));
+    load_q(t, 0);
+    ready();
+    issue_r(0);
+    bool r_pending = true;  // R of tile t issued, not yet waited for
+    if (t + 1 < t_end && head(t + 1) == head(t)) load_q(t + 1, 1);
+    for (; t < t_end; ++t, b ^= 1) {
+        const int tn = t + 1;
+        const bool has_next = tn < t_end;
+        const bool new_head = has_next && head(tn) != head(t);
+        if (r_pending && !sync_on_mma(&bar_r, phase_r, status)) break;  // R(t) complete
+        r_pending = false;
+        if (has_next && !new_head) {  // Q(t+1) was prefetched; R(t+1) runs during this epilogue
+            ready();
+            issue_r(b ^ 1);
+            r_pending = true;
+        }
+        // routes and shared-slot probabilities from this thread's row of R(t)
+        const int bh = t / tiles_per_head, q = (t % tiles_per_head) * kT + r;
+        const bool q_ok = q < N;
+        const uint32_t tR = lane_base(tmem) + b * kT;
+        float v[kT];
+        tmem_ld32(tR, v);
+        tmem_ld32(tR + 32, v + 32);
+        tmem_ld32(tR + 64, v + 64);
+        tmem_ld32(tR + 96, v + 96);
+        tmem_wait_ld();
+        uint32_t bu[SMAX];
+        int bi[SMAX];
+#pragma unroll
+        for (int u = 0; u < SMAX; ++u) { bu[u] = 0u; bi[u] = -1; }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kT; ++j) {
+            if (j < m) top_insert<SMAX>(bu, bi, order_key(v[j]), j);
+            mx = fmaxf(mx, j < m ? v[j] * sl : -INFINITY);
+        }
+        float lsum = 0.0f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int j = 0; j < kT; j += 2) {
+            const float e0 = ex2(fmaf(v[j], sl, -mx)), e1 = ex2(fmaf(v[j + 1], sl, -mx));
+            const float p0 = j < m ? e0 : 0.0f, p1 = j + 1 < m ? e1 : 0.0f;
+            lsum += p0 + p1;
+            pk[j >> 1] = pack_bf16(p0, p1);
+        }
+        tmem_store_p(tR, pk);
+        if (q_ok) {
+            int32_t* Erow = E + ((size_t)bh * N + q) * s;
+#pragma unroll
+            for (int u = 0; u < SMAX; ++u)
+                if (u < s) Erow[u] = bi[u];
+            cnt[(size_t)bh * N + q] = 0;
+        }
+        fence_before_sync();
+        __syncthreads();
+        if (r == 0) {
+            fence_after_sync();
+            issue_pv_ts<D>(tmem + kO, tmem + b * kT, smem_u32(sVt), false);
+            mma_commit(&bar_o);
+        }
+        if (!sync_on_mma(&bar_o, phase_o, status)) break;
+        {
+            float o[D];
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(lane_base(tmem) + kO + c0, o + c0);
+            tmem_wait_ld();
+            if (q_ok) {
+                const float inv = 1.0f / lsum;
+                uint4* dst = reinterpret_cast<uint4*>(sh_part + ((size_t)bh * N + q) * D);
+#pragma unroll
+                for (int u = 0; u < D / 8; ++u)
+                    dst[u] = make_uint4(pack_bf16(o[8 * u] * inv, o[8 * u + 1] * inv),
+                                        pack_bf16(o[8 * u + 2] * inv, o[8 * u + 3] * inv),
+                                        pack_bf16(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
+                                        pack_bf16(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
+                sh_lse[(size_t)bh * N + q] = mx + __log2f(lsum);
+            }
+        }
+        fence_before_sync();
+        __syncthreads();
+        if (has_next && new_head) {  // P Vt is done with this head's landmarks
+            load_landmarks(head(tn));
+            load_q(tn, b ^ 1);
+            ready();
+            issue_r(b ^ 1);
+            r_pending = true;
+        }
+        // Q(t) is consumed (R(t) done): prefetch Q(t+2) into its buffer
+        if (t + 2 < t_end && head(t + 2) == head(tn)) load_q(t + 2, b);
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (r < 32) tmem_dealloc(tmem, 512);
+}
+
 // Variant for m_pad > 256: one CTA per 128-query tile, landmarks streamed in
 // 128-row chunks into consecutive TMEM column blocks.
 template <int D, int SMAX>
@@ -656,185 +853,810 @@ __global__ void k_bucket_scatter(const int32_t* __restrict__ E, int N, int m, in
     }
 }
 
-// ------------------------------------------------------------------------
-// Expert attention, persistent over the work tiles. A tile is up to 128
-// (query, slot) pairs routed to one expert e: their queries are gathered into
-// the A tile; the keys are the shared slots (landmark keys Qt, values Vt;
-// only for slot-0 rows) followed by the k keys of I_e, 128 per chunk. Each
-// row ends with a partial (normalized bf16 output, log2-sum-exp) for its
-// (query, slot); the last of a query's s partials to finish merges them and
-// writes the output row.
+// Same grouping, one thread per (query, slot) pair, which also copies the
+// pair's query row to its bucket position in Qp, so that each work tile's
+// queries are consecutive rows there.
 template <int D>
-__global__ void __launch_bounds__(128)
-    k_expert_tc(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
+__global__ void k_bucket_scatter_copy(const int32_t* __restrict__ E, const __nv_bfloat16* __restrict__ Q, int N,
+                                      int m, int s, int* __restrict__ cursors, int32_t* __restrict__ perm,
+                                      __nv_bfloat16* __restrict__ Qp) {
+    const int bh = blockIdx.y;
+    const long long pi = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (pi >= (long long)N * s) return;
+    const int q = (int)(pi / s), t = (int)(pi % s);
+    const int e = E[((size_t)bh * N + q) * s + t];
+    if (e < 0 || e >= m) return;
+    const int pos = atomicAdd(&cursors[((size_t)bh * m + e) * 2 + (t > 0)], 1);
+    const size_t row = (size_t)bh * N * s + pos;
+    perm[row] = (q << 3) | t;
+    const uint4* src = reinterpret_cast<const uint4*>(Q + ((size_t)bh * N + q) * D);
+    uint4* dst = reinterpret_cast<uint4*>(Qp + row * D);
+    uint4 v[D / 8];
+#pragma unroll
+    for (int u = 0; u < D / 8; ++u) v[u] = src[u];
+#pragma unroll
+    for (int u = 0; u < D / 8; ++u) dst[u] = v[u];
+}
+
+// Output rows from the partials: each query's s expert partials (normalized
+// bf16 rows with log2-sum-exp) and, when given, its shared-slot partial,
+// weighted by 2^(lse - max). One thread per 8 columns of a query.
+template <int D>
+__global__ void __launch_bounds__(256) k_merge(const __nv_bfloat16* __restrict__ part, const float* __restrict__ lse,
+                                               const __nv_bfloat16* __restrict__ sh_part,
+                                               const float* __restrict__ sh_lse, __nv_bfloat16* __restrict__ O,
+                                               long long nq, int s) {
+    constexpr int G = D / 8;  // threads per query
+    const long long qi = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / G;
+    const int gcol = (threadIdx.x % G) * 8;
+    if (qi >= nq) return;
+    float lj[kMaxS + 1];
+    float L = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxS; ++j) {
+        lj[j] = j < s ? lse[qi * s + j] : -INFINITY;
+        L = fmaxf(L, lj[j]);
+    }
+    lj[kMaxS] = sh_part ? sh_lse[qi] : -INFINITY;
+    L = fmaxf(L, lj[kMaxS]);
+    uint4 raw[kMaxS + 1];
+#pragma unroll
+    for (int j = 0; j < kMaxS; ++j)
+        if (j < s) raw[j] = *reinterpret_cast<const uint4*>(part + (qi * s + j) * D + gcol);
+    if (sh_part) raw[kMaxS] = *reinterpret_cast<const uint4*>(sh_part + qi * D + gcol);
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, wsum = 0.0f;
+#pragma unroll
+    for (int j = 0; j <= kMaxS; ++j) {
+        if (j < kMaxS ? j >= s : !sh_part) continue;
+        const float w = exp2f(lj[j] - L);
+        wsum += w;
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const float2 f = __bfloat1622float2(h[v]);
+            acc[2 * v] = fmaf(w, f.x, acc[2 * v]);
+            acc[2 * v + 1] = fmaf(w, f.y, acc[2 * v + 1]);
+        }
+    }
+    const float winv = 1.0f / wsum;
+    *reinterpret_cast<uint4*>(O + qi * D + gcol) =
+        make_uint4(pack_bf16(acc[0] * winv, acc[1] * winv), pack_bf16(acc[2] * winv, acc[3] * winv),
+                   pack_bf16(acc[4] * winv, acc[5] * winv), pack_bf16(acc[6] * winv, acc[7] * winv));
+}
+
+// The last-finisher merge of a query's s partial outputs: publish this
+// partial's log2-sum-exp, count it, and if it is the query's last, combine
+// all s normalized partials (read back from L2) into the output row.
+template <int D>
+__device__ __forceinline__ void merge_partials(__nv_bfloat16* __restrict__ O, __nv_bfloat16* __restrict__ part,
+                                               float* __restrict__ lse, int* __restrict__ cnt, int bh, int N, int q,
+                                               int s, size_t pr, float my_lse) {
+    lse[pr] = my_lse;
+    // release this partial (row and lse) and, if last, acquire the others
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(cnt + (size_t)bh * N + q) : "memory");
+    if (old != s - 1) return;
+    const size_t p0 = ((size_t)bh * N + q) * s;
+    float lj[kMaxS];
+    float L = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxS; ++j) {
+        lj[j] = j < s ? __ldcg(lse + p0 + j) : -INFINITY;
+        L = fmaxf(L, lj[j]);
+    }
+    float acc[D];
+#pragma unroll
+    for (int c = 0; c < D; ++c) acc[c] = 0.0f;
+    float wsum = 0.0f;
+    for (int j = 0; j < s; ++j) {
+        const float w = exp2f(lj[j] - L);
+        wsum += w;
+        // the whole partial row in flight at once
+        const uint4* src = reinterpret_cast<const uint4*>(part + (p0 + j) * D);
+        uint4 raw[D / 8];
+#pragma unroll
+        for (int u = 0; u < D / 8; ++u) raw[u] = __ldcg(src + u);
+#pragma unroll
+        for (int u = 0; u < D / 8; ++u) {
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const float2 f = __bfloat1622float2(h[v]);
+                acc[8 * u + 2 * v] = fmaf(w, f.x, acc[8 * u + 2 * v]);
+                acc[8 * u + 2 * v + 1] = fmaf(w, f.y, acc[8 * u + 2 * v + 1]);
+            }
+        }
+    }
+    const float winv = 1.0f / wsum;
+    uint4* od = reinterpret_cast<uint4*>(O + ((size_t)bh * N + q) * D);
+#pragma unroll
+    for (int u = 0; u < D / 8; ++u)
+        od[u] = make_uint4(pack_bf16(acc[8 * u] * winv, acc[8 * u + 1] * winv),
+                           pack_bf16(acc[8 * u + 2] * winv, acc[8 * u + 3] * winv),
+                           pack_bf16(acc[8 * u + 4] * winv, acc[8 * u + 5] * winv),
+                           pack_bf16(acc[8 * u + 6] * winv, acc[8 * u + 7] * winv));
+}
+
+// ------------------------------------------------------------------------
+// Expert attention, warp-specialized and persistent (one CTA per SM).
+//   warps 0-3  softmax + epilogue, thread r <-> TMEM lane r (row r of a tile)
+//   warp 4     producer: claims work tiles, gathers the tile's queries and each
+//              chunk's keys / values (rows picked by index) with cp.async,
+//              completion counted on mbarriers
+//   warp 5     MMA issuer: S = Q K^T into one of two TMEM score buffers, and
+//              O += P V into one of two TMEM output buffers (one per tile in
+//              flight); S of chunk g+1 runs while the softmax works on chunk g
+// Shared memory: 2 query tiles and a 2-stage ring of (K, V) chunks; once S of
+// a chunk is in TMEM its K slot holds the chunk's probabilities P (bf16).
+// Every wait is bounded; a timeout sets the device status and an abort flag
+// that makes every role leave its loop.
+
+struct WsTile {
+    int bh, e, rows, shrows, nsh, nch;
+};
+
+struct WsMeta {  // what the deferred O += P V of a chunk needs
+    int st, ob, tseq;
+    bool first, last;
+};
+
+__device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > (2LL << 30)) {
+            set_status(status, kStTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    k_expert_ws(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
                 const __nv_bfloat16* __restrict__ V, const __nv_bfloat16* __restrict__ Qhi,
-                const __nv_bfloat16* __restrict__ Vtb, const int32_t* __restrict__ I, const int32_t* __restrict__ perm,
-                const int4* __restrict__ tiles, const int* __restrict__ tile_ctr, int* __restrict__ tile_next,
-                __nv_bfloat16* __restrict__ O, __nv_bfloat16* __restrict__ part, float* __restrict__ lse,
-                int* __restrict__ cnt, int N, int m, int m_pad, int k, int s, int shared_on, float sl,
-                int* __restrict__ status) {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar;
-    __shared__ uint32_t tmem_slot;
-    __shared__ int sh_tile;
-    __shared__ int rowq[kT];   // gathered query of each row (or -1)
-    __shared__ int keyj[kT];   // key row index of the current chunk (or -1)
-    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+                const __nv_bfloat16* __restrict__ Vtb, const int32_t* __restrict__ I,
+                const int32_t* __restrict__ perm, const int4* __restrict__ tiles, const int* __restrict__ tile_ctr,
+                int* __restrict__ tile_next, __nv_bfloat16* __restrict__ O, __nv_bfloat16* __restrict__ part,
+                float* __restrict__ lse, int* __restrict__ cnt, int N, int m, int m_pad, int k, int s, int shared_on,
+                float sl, int* __restrict__ status) {
     constexpr int TILE = kT * D * 2;
-    constexpr int kKP = kp_bytes<D>();
-    uint8_t* sQ = sm;
-    uint8_t* sK = sm + TILE;  // K tile, then the P tile (128 x 128 bf16)
-    uint8_t* sV = sK + kKP;
-    const int r = threadIdx.x;
-    if (r < 32) tmem_alloc(&tmem_slot, 256);
-    if (r == 0) {
-        mbar_init(&bar, 1);
+    constexpr uint32_t kS0 = 0, kO0 = 256;  // TMEM columns: S buffers 0 / 128, O buffers 256 / 384
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    constexpr int KP = kp_bytes<D>();  // K stage, later the P tile
+    uint8_t* sQ = sm;                  // 2 tiles
+    uint8_t* sK = sm + 2 * TILE;       // 2 stages of KP bytes
+    uint8_t* sV = sK + 2 * KP;         // 2 stages
+
+    __shared__ uint64_t q_full[2], q_empty[2], kv_full[2], kv_empty[2], s_full[2], s_free[2], o_full[2], o_free[2];
+    __shared__ uint64_t p_full[2], pv_done;  // p_full[g & 1]: the softmax may run two chunks ahead of O += P V
+    __shared__ WsTile tinfo[2];
+    __shared__ int rowq[2][kT];  // q << 3 | slot, or -1
+    __shared__ int keyrow[2][kT];  // producer: key rows of the chunk being loaded / the next one
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    volatile int* abort_v = &abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 5) tmem_alloc(&tmem_slot, 512);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&q_full[i], 32 + 1);  // 32 copy-completion arrivals + the row-list publish
+            mbar_init(&q_empty[i], 1 + 4);
+            mbar_init(&kv_full[i], 32);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 4);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_free[i], 4);
+        }
+        mbar_init(&p_full[0], 4);
+        mbar_init(&p_full[1], 4);
+        mbar_init(&pv_done, 1);
+        abort_flag = 0;
         fence_mbar_init();
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = tmem_slot;
-    const uint32_t tS = lane_base(tmem), tO = lane_base(tmem) + 128;
-    uint32_t phase = 0;
     const int ntiles = *(volatile const int*)tile_ctr;
-    bool ok = true;
-    for (;;) {
-        if (r == 0) sh_tile = atomicAdd(tile_next, 1);
-        __syncthreads();
-        const int t = sh_tile;
-        if (t >= ntiles) break;
-        const int4 td = tiles[t];
-        const int bh = td.x, e = td.y, start = td.z, rows = td.w & 255, shrows = td.w >> 8;
-        const int Ns = N * s;
-        int q = -1, slot = 0;
-        if (r < rows) {
-            const int pk = perm[(size_t)bh * Ns + start + r];
-            q = pk >> 3;
-            slot = pk & 7;
-        }
-        rowq[r] = q;
-        const __nv_bfloat16* Qb = Q + (size_t)bh * N * D;
-        const __nv_bfloat16* Kb = K + (size_t)bh * N * D;
-        const __nv_bfloat16* Vb = V + (size_t)bh * N * D;
-        __syncthreads();
-        load_tile<D>(smem_u32(sQ), [&](int i) { return i < 0 ? Qb : (rowq[i] >= 0 ? Qb + (size_t)rowq[i] * D : nullptr); });
-        const int nsh = (shared_on && shrows > 0) ? (m + kT - 1) / kT : 0;
-        const int nex = (k + kT - 1) / kT;
-        float mref = -INFINITY, l = 0.0f;
-        for (int c = 0; c < nsh + nex; ++c) {
-            const bool shc = c < nsh;
-            int nk;
-            const __nv_bfloat16 *kbase, *vbase;
-            if (shc) {
-                nk = min(kT, m - c * kT);
-                keyj[r] = r < nk ? c * kT + r : -1;
-                kbase = Qhi + (size_t)bh * m_pad * D;
-                vbase = Vtb + (size_t)bh * m_pad * D;
-            } else {
-                const int cc = c - nsh;
-                nk = min(kT, k - cc * kT);
-                int j = -1;
-                if (r < nk) {
-                    j = I[((size_t)bh * m + e) * k + cc * kT + r];
-                    if (j < 0 || j >= N) {
-                        set_status(status, kStBounds);
-                        j = -1;
-                    }
+    const int nex = (k + kT - 1) / kT;
+    const int nsh_full = shared_on ? (m + kT - 1) / kT : 0;
+
+    if (warp == 4) {
+        // ------------------------------------------------------- producer
+        int tseq = 0, g = 0;
+        int armed_q[2] = {0, 0}, armed_kv[2] = {0, 0};
+        for (;;) {
+            const int qs = tseq & 1;
+            int ok = 1;
+            if (lane == 0) ok = ws_wait(&q_empty[qs], ((tseq >> 1) & 1) ^ 1, status, abort_v);
+            if (lane == 0) MITA_TRACE_EV(0, 1);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            int t = 0;
+            if (lane == 0) t = atomicAdd(tile_next, 1);
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (t >= ntiles) {
+                if (lane == 0) tinfo[qs].rows = -1;
+                __syncwarp();
+                mbar_arrive(&q_full[qs]);
+                if (lane == 0) mbar_arrive(&q_full[qs]);
+                break;
+            }
+            const int4 td = tiles[t];
+            const int bh = td.x, e = td.y, start = td.z, rows = td.w & 255, shrows = td.w >> 8;
+            const int nsh = shrows > 0 ? nsh_full : 0;
+            const int nch = nsh + nex;
+            // row indices go to shared memory; the copies then run two rows per
+            // warp instruction (16 lanes x 16 bytes per 256-byte row for d = 128)
+            const int rbase = bh * N;
+            for (int r = lane; r < kT; r += 32) rowq[qs][r] = r < rows ? perm[(size_t)bh * N * s + start + r] : -1;
+            if (lane == 0) tinfo[qs] = WsTile{bh, e, rows, shrows, nsh, nch};
+            __syncwarp();
+            constexpr int CPR = D / 8;        // 16-byte chunks per row
+            constexpr int RPI = 32 / CPR;     // rows per warp instruction
+            {
+                const uint32_t dst = smem_u32(sQ + qs * TILE);
+                const int cc = lane % CPR;
+#pragma unroll 4
+                for (int r0 = 0; r0 < kT; r0 += RPI) {
+                    const int r = r0 + lane / CPR;
+                    const int pk = rowq[qs][r];
+                    const __nv_bfloat16* src = Q + ((size_t)rbase + (pk >= 0 ? (pk >> 3) : 0)) * D + cc * 8;
+                    cp_async16(dst + sw_off(r, cc, kT), src, true);
                 }
-                keyj[r] = j;
-                kbase = Kb;
-                vbase = Vb;
+                ++armed_q[qs];
+                cp_async_arrive(&q_full[qs]);
+                if (lane == 0) mbar_arrive(&q_full[qs]);  // publishes tinfo / rowq
             }
-            __syncthreads();
-            load_tile<D>(smem_u32(sK), [&](int i) { return i < 0 ? kbase : (keyj[i] >= 0 ? kbase + (size_t)keyj[i] * D : nullptr); });
-            load_tile<D>(smem_u32(sV), [&](int i) { return i < 0 ? vbase : (keyj[i] >= 0 ? vbase + (size_t)keyj[i] * D : nullptr); });
-            cp_async_wait_all();
-            fence_proxy_async();
-            __syncthreads();
-            if (r == 0) {
-                fence_after_sync();
-                issue_qk<D>(tS, smem_u32(sQ), smem_u32(sK), false);
-                mma_commit(&bar);
-            }
-            if (!(ok = sync_on_mma(&bar, phase, status))) break;
-            const bool row_ok = q >= 0 && (!shc || r < shrows);
-            CandOut none;
-            none.cand = nullptr;
-            chunk_softmax<D>(tS, tO, sK, nk, row_ok, sl, c == 0, mref, l, none);
-            fence_proxy_async();
-            fence_before_sync();
-            __syncthreads();
-            if (r == 0) {
-                fence_after_sync();
-                issue_pv<D>(tO, smem_u32(sK), smem_u32(sV), c > 0);
-                mma_commit(&bar);
-            }
-            if (!(ok = sync_on_mma(&bar, phase, status))) break;
-        }
-        if (!ok) break;
-        // epilogue: every thread reads its TMEM lane (warp-collective), valid rows store
-        const bool valid = q >= 0;
-        const float inv = valid ? 1.0f / l : 0.0f;
-        const size_t pr = valid ? ((size_t)bh * N + q) * s + slot : 0;
-        __nv_bfloat16* dst = !valid ? nullptr : (s == 1) ? O + ((size_t)bh * N + q) * D : part + pr * D;
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            float o[32];
-            tmem_ld32(tO + c0, o);
-            tmem_wait_ld();
-            if (valid) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int j = 0; j < 32; j += 2) pk[j >> 1] = pack_bf16(o[j] * inv, o[j + 1] * inv);
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    *reinterpret_cast<uint4*>(dst + c0 + 8 * u) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-            }
-        }
-        if (valid && s > 1) {
-            lse[pr] = mref + __log2f(l);
-            __threadfence();
-            const int old = atomicAdd(&cnt[(size_t)bh * N + q], 1);
-            if (old == s - 1) {
-                __threadfence();
-                const size_t p0 = ((size_t)bh * N + q) * s;
-                float L = -INFINITY;
-                for (int j = 0; j < s; ++j) L = fmaxf(L, __ldcg(lse + p0 + j));
-                float w[kMaxS], wsum = 0.0f;
-                for (int j = 0; j < s; ++j) {
-                    w[j] = exp2f(__ldcg(lse + p0 + j) - L);
-                    wsum += w[j];
-                }
-                const float winv = 1.0f / wsum;
-                __nv_bfloat16* od = O + ((size_t)bh * N + q) * D;
-#pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 8) {
-                    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                    for (int j = 0; j < s; ++j) {
-                        const uint4 raw = __ldcg(reinterpret_cast<const uint4*>(part + (p0 + j) * D + c0));
-                        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const float2 f = __bfloat1622float2(h[u]);
-                            acc[2 * u] = fmaf(w[j], f.x, acc[2 * u]);
-                            acc[2 * u + 1] = fmaf(w[j], f.y, acc[2 * u + 1]);
+            if (lane == 0) MITA_TRACE_EV(0, 2);
+            // key rows of chunk c into keyrow[buf]: landmark rows for the shared
+            // chunks, I_e entries for the expert's chunks
+            auto load_keys = [&](int c, int buf) {
+                const bool shc = c < nsh;
+                for (int r = lane; r < kT; r += 32) {
+                    int row;
+                    if (shc) {
+                        row = c * kT + r;  // < m_pad since c < ceil(m / 128)
+                    } else {
+                        const int t2 = (c - nsh) * kT + r;
+                        int j = t2 < k ? I[((size_t)bh * m + e) * k + t2] : 0;
+                        if (j < 0 || j >= N) {
+                            set_status(status, kStBounds);
+                            j = 0;
                         }
+                        row = j;
                     }
-                    *reinterpret_cast<uint4*>(od + c0) =
-                        make_uint4(pack_bf16(acc[0] * winv, acc[1] * winv), pack_bf16(acc[2] * winv, acc[3] * winv),
-                                   pack_bf16(acc[4] * winv, acc[5] * winv), pack_bf16(acc[6] * winv, acc[7] * winv));
+                    keyrow[buf][r] = row;
+                }
+            };
+            load_keys(0, g & 1);
+            bool ok2 = true;
+            for (int c = 0; c < nch; ++c, ++g) {
+                const int st = g & 1;
+                int okw = 1;
+                if (lane == 0) okw = ws_wait(&kv_empty[st], ((g >> 1) & 1) ^ 1, status, abort_v);
+                if (lane == 0) MITA_TRACE_EV(0, 3);
+                if (!__shfl_sync(0xffffffffu, okw, 0)) { ok2 = false; break; }
+                __syncwarp();
+                {
+                    const bool shc = c < nsh;
+                    const __nv_bfloat16* kb = shc ? Qhi + (size_t)bh * m_pad * D : K + (size_t)rbase * D;
+                    const __nv_bfloat16* vb = shc ? Vtb + (size_t)bh * m_pad * D : V + (size_t)rbase * D;
+                    const uint32_t dk = smem_u32(sK + st * KP), dv = smem_u32(sV + st * TILE);
+                    const int* kr = keyrow[g & 1];
+                    const int cc = lane % CPR;
+#pragma unroll 4
+                    for (int r0 = 0; r0 < kT; r0 += RPI) {
+                        const int r = r0 + lane / CPR;
+                        const size_t off = (size_t)kr[r] * D + cc * 8;
+                        cp_async16(dk + sw_off(r, cc, kT), kb + off, true);
+                        cp_async16(dv + sw_off(r, cc, kT), vb + off, true);
+                    }
+                    ++armed_kv[st];
+                    cp_async_arrive(&kv_full[st]);
+                }
+                if (lane == 0) MITA_TRACE_EV(0, 4);
+                // the next chunk's key rows load while this stage fills and the next one drains
+                if (c + 1 < nch) load_keys(c + 1, (g + 1) & 1);
+                if (lane == 0) MITA_TRACE_EV(0, 5);
+                __syncwarp();
+            }
+            if (!ok2) break;
+            ++tseq;
+        }
+        // on abort, let the copies in flight land before the CTA exits
+        if (lane == 0 && *abort_v) {
+            for (int i = 0; i < 2; ++i) {
+                if (armed_q[i]) {
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(&q_full[i], (armed_q[i] - 1) & 1) && clock64() - t0 < (1LL << 27)) {}
+                }
+                if (armed_kv[i]) {
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(&kv_full[i], (armed_kv[i] - 1) & 1) && clock64() - t0 < (1LL << 27)) {}
                 }
             }
         }
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
+    } else if (warp == 5) {
+        // ------------------------------------------------------ MMA issuer
+        // strict order: S(g), then the deferred O += P V of chunk g-1, so the
+        // tensor core computes S(g) while the softmax works on chunk g-1;
+        // every wait blocks in hardware (no spinning next to the softmax warps)
+        if (lane == 0) {
+            int g = 0, tseq = 0;
+            bool pending = false, ok = true;
+            WsMeta pm{};
+            int pg = 0;
+            auto flush_pv = [&]() -> bool {
+                if (!ws_wait(&p_full[pg & 1], (pg >> 1) & 1, status, abort_v)) return false;
+                MITA_TRACE_EV(1, 14);
+                if (pm.first && !ws_wait(&o_free[pm.ob], ((pm.tseq >> 1) & 1) ^ 1, status, abort_v)) return false;
+                fence_after_sync();
+                issue_pv<D>(tmem + kO0 + pm.ob * 128, smem_u32(sK + pm.st * KP), smem_u32(sV + pm.st * TILE),
+                            !pm.first);
+                mma_commit(&pv_done);
+                mma_commit(&kv_empty[pm.st]);
+                if (pm.last) mma_commit(&o_full[pm.ob]);
+                MITA_TRACE_EV(1, 15);
+                pending = false;
+                return true;
+            };
+            for (;;) {
+                const int qs = tseq & 1;
+                if (!(ok = ws_wait(&q_full[qs], (tseq >> 1) & 1, status, abort_v))) break;
+                MITA_TRACE_EV(1, 10);
+                const WsTile ti = tinfo[qs];
+                if (ti.rows < 0) break;
+                for (int c = 0; c < ti.nch; ++c, ++g) {
+                    const int st = g & 1, sb = g & 1;
+                    if (!(ok = ws_wait(&kv_full[st], (g >> 1) & 1, status, abort_v))) break;
+                    MITA_TRACE_EV(1, 11);
+                    if (!(ok = ws_wait(&s_free[sb], ((g >> 1) & 1) ^ 1, status, abort_v))) break;
+                    MITA_TRACE_EV(1, 12);
+                    fence_proxy_async();  // copied tiles (generic proxy) -> the MMA's async-proxy reads
+                    fence_after_sync();
+                    issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sQ + qs * TILE), smem_u32(sK + st * KP), false);
+                    mma_commit(&s_full[sb]);
+                    const bool last = c == ti.nch - 1;
+                    MITA_TRACE_EV(1, 13);
+                    if (last) mma_commit(&q_empty[qs]);
+                    if (pending && !(ok = flush_pv())) break;
+                    pending = true;
+                    pg = g;
+                    pm = WsMeta{st, tseq & 1, tseq, c == 0, last};
+                }
+                if (!ok) break;
+                ++tseq;
+            }
+            if (ok && pending) flush_pv();
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------- softmax + epilogue
+        const int r = threadIdx.x;
+        int tseq = 0, g = 0;
+        for (;;) {
+            const int qs = tseq & 1, ob = tseq & 1;
+            if (!__all_sync(0xffffffffu, ws_wait(&q_full[qs], (tseq >> 1) & 1, status, abort_v))) break;
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 20);
+            const WsTile ti = tinfo[qs];
+            if (ti.rows < 0) break;
+            const int pk = rowq[qs][r];
+            const int q = pk >= 0 ? pk >> 3 : -1, slot = pk >= 0 ? pk & 7 : 0;
+            float mref = -INFINITY, l = 0.0f;
+            bool ok = true;
+            for (int c = 0; c < ti.nch; ++c, ++g) {
+                const int sb = g & 1;
+                if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (g >> 1) & 1, status, abort_v))) { ok = false; break; }
+                if (threadIdx.x == 0) MITA_TRACE_EV(2, 21);
+                fence_after_sync();
+                const bool shc = c < ti.nsh;
+                const int nk = shc ? min(kT, m - c * kT) : min(kT, k - (c - ti.nsh) * kT);
+                const bool row_ok = q >= 0 && (!shc || r < ti.shrows);
+                const uint32_t tS = lane_base(tmem) + kS0 + sb * 128;
+                const uint32_t tO = lane_base(tmem) + kO0 + ob * 128;
+                // the whole score row in registers: four loads, one wait
+                float v[kT];
+                tmem_ld32(tS, v);
+                tmem_ld32(tS + 32, v + 32);
+                tmem_ld32(tS + 64, v + 64);
+                tmem_ld32(tS + 96, v + 96);
+                tmem_wait_ld();
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_free[sb]);  // S(g) is read: its buffer may take S(g+2)
+                if (threadIdx.x == 0) MITA_TRACE_EV(2, 22);
+                const int nval = row_ok ? nk : 0;  // columns of this row that hold a valid key
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < kT; ++j) mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
+                float mnew = mref, alpha = 1.0f;
+                if (mx > mref + 8.0f) {
+                    mnew = mx;
+                    alpha = ex2(mref - mnew);
+                }
+                uint8_t* sPg = sK + (g & 1) * KP;  // K of this chunk is consumed: P goes there
+                float sum = 0.0f;
+#pragma unroll
+                for (int c0 = 0; c0 < kT; c0 += 32) {
+                    uint32_t pkd[16];
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        // exponentiate every column, keep the valid ones (no branches)
+                        const float e0 = ex2(fmaf(v[c0 + j], sl, -mnew));
+                        const float e1 = ex2(fmaf(v[c0 + j + 1], sl, -mnew));
+                        const float p0 = c0 + j < nval ? e0 : 0.0f;
+                        const float p1 = c0 + j + 1 < nval ? e1 : 0.0f;
+                        sum += p0 + p1;
+                        pkd[j >> 1] = pack_bf16(p0, p1);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        *reinterpret_cast<uint4*>(sPg + sw_off(r, (c0 >> 3) + u, kT)) =
+                            make_uint4(pkd[4 * u], pkd[4 * u + 1], pkd[4 * u + 2], pkd[4 * u + 3]);
+                }
+                l = l * alpha + sum;
+                mref = mnew;
+                const bool resc = c > 0 && alpha != 1.0f;
+                if (__any_sync(0xffffffffu, resc)) {
+                    // O holds the previous chunk's O += P V once that MMA is done; S(g)
+                    // complete implies every MMA before it, PV(g-2) included, is done, so
+                    // this wait can only see PV(g-1)'s phase
+                    if (!__all_sync(0xffffffffu, ws_wait(&pv_done, (g - 1) & 1, status, abort_v))) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after_sync();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        float o[32];
+                        tmem_ld32(tO + c0, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] *= alpha;
+                        tmem_st32(tO + c0, o);
+                    }
+                    tmem_wait_st();
+                }
+                fence_proxy_async();
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[g & 1]);
+                if (threadIdx.x == 0) MITA_TRACE_EV(2, 24);
+            }
+            if (!ok) break;
+            // epilogue: normalized partial (or output) of each valid row
+            if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (tseq >> 1) & 1, status, abort_v))) break;
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 25);
+            fence_after_sync();
+            const uint32_t tO = lane_base(tmem) + kO0 + ob * 128;
+            const bool valid = q >= 0;
+            const int bh = ti.bh;
+            const float inv = valid ? 1.0f / l : 0.0f;
+            const size_t pr = valid ? ((size_t)bh * N + q) * s + slot : 0;
+            __nv_bfloat16* dst = !valid ? nullptr : (s == 1) ? O + ((size_t)bh * N + q) * D : part + pr * D;
+            {
+                float o[D];
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(tO + c0, o + c0);
+                tmem_wait_ld();
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&o_free[ob]);   // O is read: the tile after next may accumulate into it
+                    mbar_arrive(&q_empty[qs]);  // row list and query tile no longer needed
+                }
+                if (valid) {
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 8)
+                        *reinterpret_cast<uint4*>(dst + c0) =
+                            make_uint4(pack_bf16(o[c0] * inv, o[c0 + 1] * inv), pack_bf16(o[c0 + 2] * inv, o[c0 + 3] * inv),
+                                       pack_bf16(o[c0 + 4] * inv, o[c0 + 5] * inv), pack_bf16(o[c0 + 6] * inv, o[c0 + 7] * inv));
+                }
+            }
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 26);
+            if (valid && s > 1) merge_partials<D>(O, part, lse, cnt, bh, N, q, s, pr, mref + __log2f(l));
+            ++tseq;
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 27);
+        }
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (r < 32) tmem_dealloc(tmem, 256);
+    if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------------
+// Expert attention with the expert's keys and values resident in shared
+// memory (k <= 256): each CTA walks a contiguous range of work tiles; the
+// tiles of one expert are adjacent, so K_(e), V_(e) are gathered once per
+// expert and reused by all its tiles. The shared slots come in as a separate
+// partial (routing kernel). Roles as in k_expert_ws; the probabilities are
+// written over the scores in TMEM and O += P V reads them from there.
+struct ResTile {
+    int bh, e, rows, gen;  // gen: loads of the resident keys so far (this tile uses load gen - 1)
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    k_expert_res(const __grid_constant__ CUtensorMap tmQp, const __nv_bfloat16* __restrict__ K,
+                 const __nv_bfloat16* __restrict__ V, const int32_t* __restrict__ I, const int32_t* __restrict__ perm,
+                 const int4* __restrict__ tiles, const int* __restrict__ tile_ctr, __nv_bfloat16* __restrict__ part,
+                 float* __restrict__ lse, int N, int m, int k, int s, float sl, int* __restrict__ status) {
+    constexpr int TILE = kT * D * 2;
+    constexpr uint32_t kS0 = 0, kO0 = 256;  // TMEM: S/P buffers 0 / 128, O buffers 256 / 384
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sQ = sm;             // 2 query tiles
+    uint8_t* sK = sm + 2 * TILE;  // resident key chunks (up to 2)
+    uint8_t* sV = sm + 4 * TILE;  // resident value chunks
+
+    __shared__ uint64_t q_full[2], q_empty[2], kv_full[2], kv_free[2], s_full[2], p_full[2], o_full[2], o_free[2];
+    __shared__ uint64_t pv_done;
+    __shared__ ResTile tinfo[2];
+    __shared__ int rowq[2][kT];
+    __shared__ int keyrow[kT];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    volatile int* abort_v = &abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = *(volatile const int*)tile_ctr;
+    const int per = (ntiles + gridDim.x - 1) / gridDim.x;
+    const int t_begin = blockIdx.x * per, t_end = min(ntiles, t_begin + per);
+    const int nloc = max(0, t_end - t_begin);
+    if (nloc == 0) return;
+    const int nex = (k + kT - 1) / kT;  // <= 2
+    if (warp == 5) tmem_alloc(&tmem_slot, 512);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1 + 4);
+            mbar_init(&kv_full[i], 32);
+            mbar_init(&kv_free[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_free[i], 4);
+        }
+        mbar_init(&pv_done, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    constexpr int CPR = D / 8, RPI = 32 / CPR;  // 16-byte chunks per row, rows per warp instruction
+
+    if (warp == 4) {
+        // ------------------------------------------------------- producer
+        int cur_bh = -1, cur_e = -1, gen = 0;
+        int armed_q[2] = {0, 0}, armed_kv[2] = {0, 0};
+        const int cc = lane % CPR;
+        for (int tl = 0; tl < nloc; ++tl) {
+            const int qs = tl & 1;
+            int ok = 1;
+            if (lane == 0) ok = ws_wait(&q_empty[qs], ((tl >> 1) & 1) ^ 1, status, abort_v);
+            if (lane == 0) MITA_TRACE_EV(0, 1);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            const int4 td = tiles[t_begin + tl];
+            const int bh = td.x, e = td.y, start = td.z, rows = td.w & 255;
+            const bool reload = bh != cur_bh || e != cur_e;
+            for (int r = lane; r < kT; r += 32) rowq[qs][r] = r < rows ? perm[(size_t)bh * N * s + start + r] : -1;
+            if (lane == 0) tinfo[qs] = ResTile{bh, e, rows, gen + (reload ? 1 : 0)};
+            __syncwarp();
+            if (lane == 0) {  // the tile's queries are consecutive rows of Qp: one bulk copy per 64 columns
+                mbar_expect_tx(&q_full[qs], TILE);  // also publishes tinfo / rowq
+                ++armed_q[qs];
+                const int y = bh * N * s + start;
+#pragma unroll
+                for (int cb = 0; cb < D / 64; ++cb)
+                    tma_load_2d(smem_u32(sQ + qs * TILE) + cb * kT * 128, &tmQp, cb * 64, y, &q_full[qs]);
+            }
+            if (lane == 0) MITA_TRACE_EV(0, 2);
+            if (reload) {
+                const __nv_bfloat16* Kb = K + (size_t)bh * N * D;
+                const __nv_bfloat16* Vb = V + (size_t)bh * N * D;
+                const int32_t* Ie = I + ((size_t)bh * m + e) * k;
+                bool okc = true;
+                for (int c = 0; c < nex; ++c) {
+                    // the previous tile's O += P V on this chunk must be done (tiles before it are)
+                    if (tl > 0) {
+                        int okw = 1;
+                        if (lane == 0) okw = ws_wait(&kv_free[c], (tl - 1) & 1, status, abort_v);
+                        if (!__shfl_sync(0xffffffffu, okw, 0)) { okc = false; break; }
+                    }
+                    for (int r = lane; r < kT; r += 32) {
+                        const int t2 = c * kT + r;
+                        int j = t2 < k ? Ie[t2] : 0;
+                        if (j < 0 || j >= N) {
+                            set_status(status, kStBounds);
+                            j = 0;
+                        }
+                        keyrow[r] = j;
+                    }
+                    __syncwarp();
+                    const uint32_t dk = smem_u32(sK + c * TILE), dv = smem_u32(sV + c * TILE);
+#pragma unroll 4
+                    for (int r0 = 0; r0 < kT; r0 += RPI) {
+                        const int r = r0 + lane / CPR;
+                        const size_t off = (size_t)keyrow[r] * D + cc * 8;
+                        cp_async16(dk + sw_off(r, cc, kT), Kb + off, true);
+                        cp_async16(dv + sw_off(r, cc, kT), Vb + off, true);
+                    }
+                    ++armed_kv[c];
+                    cp_async_arrive(&kv_full[c]);
+                    if (lane == 0) MITA_TRACE_EV(0, 4);
+                    __syncwarp();
+                }
+                if (!okc) break;
+                ++gen;
+                cur_bh = bh;
+                cur_e = e;
+            }
+        }
+        cp_async_wait_all();  // nothing of ours may still be in flight when the CTA exits
+    } else if (warp == 5) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int g = 0, cur_gen = 0;
+            bool pending = false, ok = true;
+            int pg = 0, pc = 0, pob = 0, ptl = 0;
+            bool pfirst = false, plast = false;
+            auto flush_pv = [&]() -> bool {
+                if (!ws_wait(&p_full[pg & 1], (pg >> 1) & 1, status, abort_v)) return false;
+                MITA_TRACE_EV(1, 14);
+                if (pfirst && !ws_wait(&o_free[pob], ((ptl >> 1) & 1) ^ 1, status, abort_v)) return false;
+                fence_after_sync();
+                issue_pv_ts<D>(tmem + kO0 + pob * 128, tmem + kS0 + (pg & 1) * 128, smem_u32(sV + pc * TILE), !pfirst);
+                mma_commit(&pv_done);
+                mma_commit(&kv_free[pc]);
+                if (plast) mma_commit(&o_full[pob]);
+                MITA_TRACE_EV(1, 15);
+                pending = false;
+                return true;
+            };
+            for (int tl = 0; tl < nloc && ok; ++tl) {
+                const int qs = tl & 1;
+                if (!(ok = ws_wait(&q_full[qs], (tl >> 1) & 1, status, abort_v))) break;
+                MITA_TRACE_EV(1, 10);
+                const int gen = tinfo[qs].gen;
+                // a reload waits for the previous tile's last O += P V: issue it now
+                if (pending && gen != cur_gen && !(ok = flush_pv())) break;
+                cur_gen = gen;
+                for (int c = 0; c < nex; ++c, ++g) {
+                    if (!(ok = ws_wait(&kv_full[c], (gen - 1) & 1, status, abort_v))) break;
+                    MITA_TRACE_EV(1, 11);
+                    fence_proxy_async();  // copied tiles (generic proxy) -> the MMA's async-proxy reads
+                    fence_after_sync();
+                    const int sb = g & 1;
+                    issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sQ + qs * TILE), smem_u32(sK + c * TILE), false);
+                    mma_commit(&s_full[sb]);
+                    const bool last = c == nex - 1;
+                    MITA_TRACE_EV(1, 13);
+                    if (last) mma_commit(&q_empty[qs]);
+                    if (pending && !(ok = flush_pv())) break;
+                    pending = true;
+                    pg = g;
+                    pc = c;
+                    pob = tl & 1;
+                    ptl = tl;
+                    pfirst = c == 0;
+                    plast = last;
+                }
+            }
+            if (ok && pending) flush_pv();
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------- softmax + epilogue
+        const int r = threadIdx.x;
+        int g = 0;
+        for (int tl = 0; tl < nloc; ++tl) {
+            const int qs = tl & 1, ob = tl & 1;
+            if (!__all_sync(0xffffffffu, ws_wait(&q_full[qs], (tl >> 1) & 1, status, abort_v))) break;
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 20);
+            const ResTile ti = tinfo[qs];
+            const int pk = rowq[qs][r];
+            const int q = pk >= 0 ? pk >> 3 : -1, slot = pk >= 0 ? pk & 7 : 0;
+            float mref = -INFINITY, l = 0.0f;
+            bool ok = true;
+            const uint32_t tO = lane_base(tmem) + kO0 + ob * 128;
+            for (int c = 0; c < nex; ++c, ++g) {
+                const int sb = g & 1;
+                if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (g >> 1) & 1, status, abort_v))) { ok = false; break; }
+                if (threadIdx.x == 0) MITA_TRACE_EV(2, 21);
+                fence_after_sync();
+                const uint32_t tS = lane_base(tmem) + kS0 + sb * 128;
+                const int nval = q >= 0 ? min(kT, k - c * kT) : 0;
+                float v[kT];
+                tmem_ld32(tS, v);
+                tmem_ld32(tS + 32, v + 32);
+                tmem_ld32(tS + 64, v + 64);
+                tmem_ld32(tS + 96, v + 96);
+                tmem_wait_ld();
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < kT; ++j) mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
+                float mnew = mref, alpha = 1.0f;
+                if (mx > mref + 8.0f) {
+                    mnew = mx;
+                    alpha = ex2(mref - mnew);
+                }
+                float sum = 0.0f;
+                uint32_t pkd[64];
+#pragma unroll
+                for (int j = 0; j < kT; j += 2) {
+                    const float e0 = ex2(fmaf(v[j], sl, -mnew)), e1 = ex2(fmaf(v[j + 1], sl, -mnew));
+                    const float p0 = j < nval ? e0 : 0.0f, p1 = j + 1 < nval ? e1 : 0.0f;
+                    sum += p0 + p1;
+                    pkd[j >> 1] = pack_bf16(p0, p1);
+                }
+                tmem_store_p(tS, pkd);  // P over this row's scores
+                if (threadIdx.x == 0) MITA_TRACE_EV(2, 22);
+                l = l * alpha + sum;
+                mref = mnew;
+                if (__any_sync(0xffffffffu, c > 0 && alpha != 1.0f)) {
+                    // S(g) done implies PV(g-2) done: this wait can only see PV(g-1)'s phase
+                    if (!__all_sync(0xffffffffu, ws_wait(&pv_done, (g - 1) & 1, status, abort_v))) { ok = false; break; }
+                    fence_after_sync();
+                    const float a = (c > 0) ? alpha : 1.0f;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        float o[32];
+                        tmem_ld32(tO + c0, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] *= a;
+                        tmem_st32(tO + c0, o);
+                    }
+                    tmem_wait_st();
+                }
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[g & 1]);
+            }
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 24);
+            if (!ok) break;
+            if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (tl >> 1) & 1, status, abort_v))) break;
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 25);
+            fence_after_sync();
+            float o[D];
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(tO + c0, o + c0);
+            tmem_wait_ld();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&o_free[ob]);
+                mbar_arrive(&q_empty[qs]);
+            }
+            if (q >= 0) {  // normalized partial of this (query, slot); the merge kernel combines them
+                const size_t pr = ((size_t)ti.bh * N + q) * s + slot;
+                const float inv = 1.0f / l;
+                uint4* dst = reinterpret_cast<uint4*>(part + pr * D);
+#pragma unroll
+                for (int u = 0; u < D / 8; ++u)
+                    dst[u] = make_uint4(pack_bf16(o[8 * u] * inv, o[8 * u + 1] * inv),
+                                        pack_bf16(o[8 * u + 2] * inv, o[8 * u + 3] * inv),
+                                        pack_bf16(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
+                                        pack_bf16(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
+                lse[pr] = mref + __log2f(l);
+            }
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 27);
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (warp == 5) tmem_dealloc(tmem, 512);
 }
 
 // ------------------------------------------------------------------ host
@@ -875,11 +1697,44 @@ TcPlan tc_plan(const Dims& D) {
     p.R = R;
     p.n_samp = (D.N + R - 1) / R;
     p.cand_cap = (long long)p.chunks_per_split * kT;
+    p.resident = D.shared && p.m_pad == kT && D.k <= 2 * kT;
     return p;
 }
 
 bool tc_supported(const Dims& D) {
     return D.dtype == 1 && (D.d == 64 || D.d == 128) && D.m <= 512 && D.N <= (1 << 20);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    }
+    return fn;
+}
+
+// Tensor map over `rows` rows of D bf16 (row-major) read in boxes of 64
+// columns x 128 rows with the 128-byte swizzle (the operand tile layout).
+static cudaError_t tile_map(CUtensorMap* map, const void* base, long long rows, int D) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kT};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <typename F>
@@ -892,7 +1747,16 @@ static cudaError_t launch_route_s(const Dims& D, const TcPlan& P, const TcWork& 
                                   int32_t* E, int* status, cudaStream_t st) {
     cudaError_t e;
     const int tile = kT * DD * 2;
-    if (P.m_pad <= 256) {
+    if (P.resident) {  // routes + the shared-slot partial in one pass
+        const int smem = 5 * tile + 1024;
+        if ((e = set_smem(k_route_shared_tc<DD, SMAX>, smem))) return e;
+        const int tph = (D.N + kT - 1) / kT;
+        const int total = tph * D.BH;
+        const int grid = std::min(total, num_sms());
+        k_route_shared_tc<DD, SMAX><<<grid, 128, smem, st>>>(q, W.Qhi, W.Qlo, W.Vtb, D.N, D.m, D.s, tph, total,
+                                                             D.scale * 1.4426950408889634f, E, W.cnt, W.sh_part,
+                                                             W.sh_lse, status);
+    } else if (P.m_pad <= 256) {
         const int smem = 2 * P.m_pad * DD * 2 + 2 * tile + 1024;
         if ((e = set_smem(k_route_tc<DD, SMAX>, smem))) return e;
         const int tph = (D.N + kT - 1) / kT;
@@ -977,18 +1841,38 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
         dim3 grid((D.N + 255) / 256, D.BH);
         k_bucket_count<<<grid, 256, use_smem ? 8 * D.m : 0, st>>>(E, D.N, D.m, D.s, W.counts, use_smem, status);
         k_bucket_scan<<<D.BH, 512, 0, st>>>(W.counts, D.m, D.N * D.s, W.cursors, W.toff, W.tile_ctr, W.tiles);
-        k_bucket_scatter<<<grid, 256, 0, st>>>(E, D.N, D.m, D.s, W.cursors, W.perm);
+        if (P.resident) {
+            dim3 g2((unsigned)(((long long)D.N * D.s + 255) / 256), D.BH);
+            k_bucket_scatter_copy<DD><<<g2, 256, 0, st>>>(E, q, D.N, D.m, D.s, W.cursors, W.perm, W.Qp);
+        } else {
+            k_bucket_scatter<<<grid, 256, 0, st>>>(E, D.N, D.m, D.s, W.cursors, W.perm);
+        }
         if ((e = cudaGetLastError())) return e;
         count_launch(3);
     }
     // expert attention + merge
     prof_mark(st, "expert");
     {
-        const int smem = std::max(2 * tile + kp_bytes<DD>(), 100 * 1024) + 1024;
-        if ((e = set_smem(k_expert_tc<DD>, smem))) return e;
-        k_expert_tc<DD><<<2 * num_sms(), 128, smem, st>>>(q, kk, v, W.Qhi, W.Vtb, I, W.perm, W.tiles, W.tile_ctr,
+        if (P.resident) {
+            alignas(64) CUtensorMap mq;
+            if ((e = tile_map(&mq, W.Qp, (long long)D.BH * D.N * D.s, DD))) return e;
+            const int smem = 6 * tile + 1024;
+            if ((e = set_smem(k_expert_res<DD>, smem))) return e;
+            k_expert_res<DD><<<num_sms(), 192, smem, st>>>(mq, kk, v, I, W.perm, W.tiles, W.tile_ctr, W.part, W.lse,
+                                                           D.N, D.m, D.k, D.s, sl, status);
+            if ((e = cudaGetLastError())) return e;
+            count_launch();
+            prof_mark(st, "merge");
+            const long long nq = (long long)D.BH * D.N;
+            k_merge<DD><<<(unsigned)((nq * (DD / 8) + 255) / 256), 256, 0, st>>>(W.part, W.lse, W.sh_part, W.sh_lse,
+                                                                               (__nv_bfloat16*)O, nq, D.s);
+        } else {
+            const int smem = 4 * tile + 2 * kp_bytes<DD>() + 1024;
+            if ((e = set_smem(k_expert_ws<DD>, smem))) return e;
+            k_expert_ws<DD><<<num_sms(), 192, smem, st>>>(q, kk, v, W.Qhi, W.Vtb, I, W.perm, W.tiles, W.tile_ctr,
                                                           W.tile_ctr + 1, (__nv_bfloat16*)O, W.part, W.lse, W.cnt,
                                                           D.N, D.m, P.m_pad, D.k, D.s, D.shared ? 1 : 0, sl, status);
+        }
         if ((e = cudaGetLastError())) return e;
         count_launch();
     }
@@ -1003,3 +1887,15 @@ cudaError_t launch_forward_tc(const Dims& D, const TcPlan& P, const TcWork& W, c
 }
 
 }  // namespace mita
+
+#ifdef MITA_TRACE
+// Trace builds only: copies the event logs out and clears them.
+extern "C" int mita_trace_read(unsigned long long* host, int* counts) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    cudaMemcpyFromSymbol(host, mita::g_mita_trace, sizeof(unsigned long long) * 4 * mita::kTraceCap);
+    cudaMemcpyFromSymbol(counts, mita::g_mita_trace_n, sizeof(int) * 4);
+    int zero[4] = {0, 0, 0, 0};
+    cudaMemcpyToSymbol(mita::g_mita_trace_n, zero, sizeof zero);
+    return 0;
+}
+#endif

@@ -80,13 +80,14 @@ def run_gpu(w, Qn, Kn, Vn, flags=0, scale=0.0):
     import compressed_attention_adaptive_gb300 as mita
     Q, K, V = (to_torch(a, w.dtype) for a in (Qn, Kn, Vn))
     grid = w.grid if w.grid else None
-    O, idx, route, Vt = mita.forward(Q, K, V, w.m, w.k, w.s, grid=grid, lm=w.lm, scale=scale, flags=flags,
-                                     return_sets=True)
     p = mita.params_for(Q, w.m, w.k, w.s, grid, w.lm, scale, flags)
+    ws = mita.workspace(p)
+    O, idx, route, Vt = mita.forward(Q, K, V, w.m, w.k, w.s, grid=grid, lm=w.lm, scale=scale, flags=flags,
+                                     return_sets=True, ws=ws)
+    mita.mita_device_status(ws)  # raises on a device-side timeout or index error
     Qt = torch.empty((w.B, w.H, w.m, w.d), dtype=torch.float32, device=Q.device)
-    mita.mita_landmarks(p, Q, Qt, mita.workspace(p))
-    torch.cuda.synchronize()
-    mita.mita_device_status(mita.workspace(p))
+    mita.mita_landmarks(p, Q, Qt, ws)
+    mita.mita_device_status(ws)
     return {"O": from_torch(O), "I": idx.cpu().numpy(), "E": route.cpu().numpy(), "Vt": from_torch(Vt),
             "Qt": from_torch(Qt)}
 
