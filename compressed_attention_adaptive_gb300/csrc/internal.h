@@ -33,7 +33,7 @@ cudaError_t launch_topk_dense(const float* S, long long rows, int N, int k, int3
 cudaError_t launch_sample_threshold(const float* Ssamp, long long rows, int n_samp, int k, float* thr,
                                     cudaStream_t st);
 cudaError_t launch_topk_cand(const int2* cand, const int* ccount, int splits, long long cap, int BH, int m, int m_pad,
-                             int N, int k, int32_t* I, int* status, cudaStream_t st);
+                             int N, int k, long long expect, int32_t* I, int* status, cudaStream_t st);
 
 }  // namespace mita
 

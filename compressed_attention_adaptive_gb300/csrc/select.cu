@@ -9,6 +9,8 @@
 // the keys equal to v are still needed; one ordered pass then keeps every
 // score above v and the first needed ones equal to v, so the output comes out
 // ascending without a sort.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -98,60 +100,50 @@ __global__ void __launch_bounds__(512) k_sample_threshold(const float* __restric
     }
 }
 
-// Candidates of one row: `splits` regions of (score, key) records, region sp
-// holding counts[sp] records at base + sp * cap.
-struct CandRow {
+// Candidates of one row as (order key, key index) pairs: either staged in
+// shared memory (n of them) or read from the `splits` record regions in
+// global memory (region sp holding counts[sp] records at base + sp * cap).
+struct CandSrc {
+    const uint32_t* skey;
+    const int* sidx;
+    int n;
     const int2* base;
     const int* counts;
     int splits;
     long long cap;
     template <typename F> __device__ __forceinline__ void each(F f) const {
-        for (int sp = 0; sp < splits; ++sp) {
-            const int c = counts[sp];
-            const int2* b = base + sp * cap;
-            for (int t = threadIdx.x; t < c; t += blockDim.x) f(b[t]);
+        if (skey) {
+            for (int t = threadIdx.x; t < n; t += blockDim.x) f(skey[t], sidx[t]);
+        } else {
+            for (int sp = 0; sp < splits; ++sp) {
+                const int c = counts[sp];
+                const int2* b = base + sp * cap;
+                for (int t = threadIdx.x; t < c; t += blockDim.x) {
+                    const int2 r = b[t];
+                    f(order_key(__int_as_float(r.x)), r.y);
+                }
+            }
         }
     }
 };
 
-// Exact top-k of one landmark row from its candidates: radix select of the
-// k-th largest score, the lowest key indices among scores equal to it, then
-// the chosen keys marked in a bitmap and written out in ascending order.
-// Dynamic shared memory: ceil(N / 32) words.
-__global__ void __launch_bounds__(512) k_topk_cand(const int2* __restrict__ cand, const int* __restrict__ ccount,
-                                                   int splits, long long cap, int m, int m_pad, int N, int k,
-                                                   int32_t* __restrict__ I, int* __restrict__ status) {
-    extern __shared__ uint32_t bits[];
-    __shared__ unsigned hist[256];
-    __shared__ int tmp[33];
+// MSD radix select over the candidates: the largest key v such that at least
+// `rem` candidates (those key_of accepts) are >= v, as 4 passes of 8-bit
+// digits. Returns v, the count of that key still needed (*rem_out) and how
+// many candidates have it (*eq_out).
+template <typename KeyOf>
+__device__ __forceinline__ uint32_t radix_select(const CandSrc& cs, int rem, KeyOf key_of, unsigned* hist,
+                                                 int* rem_out, int* eq_out) {
     __shared__ uint32_t sh_prefix;
-    __shared__ int sh_rem, sh_total, sh_eq;
-    const int bh = blockIdx.y, i = blockIdx.x;
-    const size_t rrow = (size_t)bh * m_pad + i;
-    CandRow cr{cand + rrow * splits * cap, ccount + rrow * splits, splits, cap};
-    const int nwords = (N + 31) >> 5;
-    for (int w = threadIdx.x; w < nwords; w += blockDim.x) bits[w] = 0u;
-    if (threadIdx.x == 0) {
-        int tot = 0;
-        for (int sp = 0; sp < splits; ++sp) tot += ccount[rrow * splits + sp];
-        sh_total = tot;
-    }
-    __syncthreads();
-    int32_t* dst = I + ((size_t)bh * m + i) * k;
-    if (sh_total < k) {  // cannot happen when the threshold holds; flag it
-        if (threadIdx.x == 0) set_status(status, kStBounds);
-        for (int t = threadIdx.x; t < k; t += blockDim.x) dst[t] = t;
-        return;
-    }
-    // k-th largest score key v, and how many keys equal to v are needed (rem)
+    __shared__ int sh_rem, sh_eq;
     uint32_t prefix = 0u, mask = 0u;
-    int rem = k;
     for (int shift = 24; shift >= 0; shift -= 8) {
         for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0u;
         __syncthreads();
-        cr.each([&](int2 c) {
-            const uint32_t u = order_key(__int_as_float(c.x));
-            if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+        cs.each([&](uint32_t u0, int j) {
+            bool ok;
+            const uint32_t u = key_of(u0, j, &ok);
+            if (ok && (u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
         });
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -169,44 +161,78 @@ __global__ void __launch_bounds__(512) k_topk_cand(const int2* __restrict__ cand
         rem = sh_rem;
         mask |= 0xFFu << shift;
     }
-    const uint32_t v = prefix;
-    const int n_eq = sh_eq;  // keys equal to v among the candidates
-    // among keys equal to v keep the rem lowest indices: the rem-th largest of ~index
-    uint32_t idx_cut = 0xFFFFFFFFu;  // ~index >= idx_cut  <=> index <= ~idx_cut
-    if (rem < n_eq) {
-        uint32_t p2 = 0u, m2 = 0u;
-        int r2 = rem;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0u;
-            __syncthreads();
-            cr.each([&](int2 c) {
-                if (order_key(__int_as_float(c.x)) != v) return;
-                const uint32_t u = ~(uint32_t)c.y;
-                if ((u & m2) == p2) atomicAdd(&hist[(u >> shift) & 255u], 1u);
-            });
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                int acc = 0, b = 255;
-                for (; b > 0; --b) {
-                    if (acc + (int)hist[b] >= r2) break;
-                    acc += (int)hist[b];
-                }
-                sh_prefix = p2 | ((uint32_t)b << shift);
-                sh_rem = r2 - acc;
-            }
-            __syncthreads();
-            p2 = sh_prefix;
-            r2 = sh_rem;
-            m2 |= 0xFFu << shift;
+    *rem_out = rem;
+    *eq_out = sh_eq;
+    return prefix;
+}
+
+// Exact top-k of one landmark row from its candidates: the k-th largest score
+// key v, the lowest key indices among scores equal to v, then the chosen keys
+// marked in a bitmap and written out in ascending order. Dynamic shared
+// memory: ceil(N / 32) bitmap words, then room for `stage_cap` staged
+// candidates (key and index arrays); rows with more candidates are read from
+// global memory on every pass instead.
+__global__ void __launch_bounds__(512) k_topk_cand(const int2* __restrict__ cand, const int* __restrict__ ccount,
+                                                   int splits, long long cap, int m, int m_pad, int N, int k,
+                                                   int stage_cap, int32_t* __restrict__ I, int* __restrict__ status) {
+    extern __shared__ uint32_t dyn[];
+    __shared__ unsigned hist[256];
+    __shared__ int tmp[33];
+    __shared__ int sh_off[65];
+    __shared__ int sh_total;
+    const int bh = blockIdx.y, i = blockIdx.x;
+    const size_t rrow = (size_t)bh * m_pad + i;
+    const int nwords = (N + 31) >> 5;
+    uint32_t* bits = dyn;
+    uint32_t* skey = dyn + nwords;
+    int* sidx = reinterpret_cast<int*>(skey + stage_cap);
+    const int* cnts = ccount + rrow * splits;
+    const int2* base = cand + rrow * splits * cap;
+    for (int w = threadIdx.x; w < nwords; w += blockDim.x) bits[w] = 0u;
+    if (threadIdx.x == 0) {
+        int tot = 0;
+        for (int sp = 0; sp < splits; ++sp) {
+            if (sp < 64) sh_off[sp] = tot;
+            tot += cnts[sp];
         }
-        idx_cut = p2;
-    } else {
-        idx_cut = 0u;  // take every key equal to v
+        sh_total = tot;
     }
-    cr.each([&](int2 c) {
-        const uint32_t u = order_key(__int_as_float(c.x));
-        const bool take = u > v || (u == v && ~(uint32_t)c.y >= idx_cut);
-        if (take && c.y >= 0 && c.y < N) atomicOr(&bits[c.y >> 5], 1u << (c.y & 31));
+    __syncthreads();
+    const int total = sh_total;
+    int32_t* dst = I + ((size_t)bh * m + i) * k;
+    if (total < k) {  // cannot happen when the threshold holds; flag it
+        if (threadIdx.x == 0) set_status(status, kStBounds);
+        for (int t = threadIdx.x; t < k; t += blockDim.x) dst[t] = t;
+        return;
+    }
+    CandSrc cs{nullptr, nullptr, 0, base, cnts, splits, cap};
+    if (total <= stage_cap && splits <= 64) {  // one read of the records, the passes run in shared memory
+        for (int sp = 0; sp < splits; ++sp) {
+            const int c = cnts[sp], o = sh_off[sp];
+            const int2* b = base + sp * cap;
+            for (int t = threadIdx.x; t < c; t += blockDim.x) {
+                const int2 r = b[t];
+                skey[o + t] = order_key(__int_as_float(r.x));
+                sidx[o + t] = r.y;
+            }
+        }
+        __syncthreads();
+        cs.skey = skey;
+        cs.sidx = sidx;
+        cs.n = total;
+    }
+    int rem, n_eq;
+    const uint32_t v = radix_select(cs, k, [](uint32_t u, int, bool* ok) { *ok = true; return u; }, hist, &rem, &n_eq);
+    // among keys equal to v keep the rem lowest indices: the rem-th largest of ~index
+    uint32_t idx_cut = 0u;  // take every key equal to v
+    if (rem < n_eq) {
+        int r2, e2;
+        idx_cut = radix_select(cs, rem, [v](uint32_t u, int j, bool* ok) { *ok = (u == v); return ~(uint32_t)j; },
+                               hist, &r2, &e2);
+    }
+    cs.each([&](uint32_t u, int j) {
+        const bool take = u > v || (u == v && ~(uint32_t)j >= idx_cut);
+        if (take && j >= 0 && j < N) atomicOr(&bits[j >> 5], 1u << (j & 31));
     });
     __syncthreads();
     // ascending write-out
@@ -237,13 +263,16 @@ cudaError_t launch_sample_threshold(const float* Ssamp, long long rows, int n_sa
 }
 
 cudaError_t launch_topk_cand(const int2* cand, const int* ccount, int splits, long long cap, int BH, int m, int m_pad,
-                             int N, int k, int32_t* I, int* status, cudaStream_t st) {
-    const int smem = ((N + 31) / 32) * 4;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k_topk_cand, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-    }
-    k_topk_cand<<<dim3(m, BH), 512, smem, st>>>(cand, ccount, splits, cap, m, m_pad, N, k, I, status);
+                             int N, int k, long long expect, int32_t* I, int* status, cudaStream_t st) {
+    const int bitmap = ((N + 31) / 32) * 4;
+    // stage about three times the expected candidate count (8k at most) so
+    // that several rows fit on an SM; larger rows read from global memory
+    const long long want = std::min<long long>(8192, std::max<long long>(1024, 3 * expect));
+    const int stage_cap = (int)std::max<long long>(0, std::min<long long>(want, (160 * 1024 - bitmap) / 8));
+    const int smem = bitmap + stage_cap * 8;
+    cudaError_t e0 = cudaFuncSetAttribute(k_topk_cand, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e0 != cudaSuccess) return e0;
+    k_topk_cand<<<dim3(m, BH), 512, smem, st>>>(cand, ccount, splits, cap, m, m_pad, N, k, stage_cap, I, status);
     count_launch();
     return cudaGetLastError();
 }

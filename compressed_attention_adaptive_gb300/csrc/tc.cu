@@ -43,7 +43,8 @@ constexpr int kPTile = kT * kT * 2;         // P tile bytes (128 x 128 bf16)
 template <int D> constexpr int kp_bytes() { return kT * D * 2 > kPTile ? kT * D * 2 : kPTile; }
 constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);  // S[128 x 128] = A[128 x d] B[128 x d]^T
 
-__device__ __forceinline__ uint32_t lane_base(uint32_t tmem) { return tmem + ((threadIdx.x & ~31u) << 16); }
+__device__ __forceinline__ uint32_t lane_base(uint32_t tmem) { return tmem + ((threadIdx.x & 96u) << 16); }
+
 
 // Thread 0 waits on the MMA barrier; everyone then syncs. Returns false (for
 // all threads) if the wait ran out.
@@ -314,7 +315,9 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // Sample pass of the top-k selection: raw scores of each landmark row against
-// every R-th key (n_samp keys), same MMA sequence as the landmark pass.
+// a sample of the keys (runs of 16 consecutive keys, one run every 16R keys;
+// n_samp slots, those past the last key scored -inf), same MMA sequence as
+// the landmark pass.
 template <int D>
 __global__ void __launch_bounds__(128)
     k_sample_tc(const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ Qhi,
@@ -347,8 +350,12 @@ __global__ void __launch_bounds__(128)
     const int row = mt * kT + r;
     for (int c = cg * chunks_per_cta; c < (cg + 1) * chunks_per_cta && c * kT < n_samp; ++c) {
         const int t0 = c * kT, nk = min(kT, n_samp - t0);
+        // sample t is key (t / 16) * 16R + t % 16: runs of 16 consecutive keys
         load_tile<D>(smem_u32(sK), [&](int t) {
-            return (t >= 0 && t < nk) ? Kb + (size_t)(t0 + t) * R * D : (t < 0 ? Kb : nullptr);
+            if (t < 0) return Kb;
+            const int u = t0 + t;
+            const long long j = (long long)(u >> 4) * 16 * R + (u & 15);
+            return (t < nk && j < N) ? Kb + (size_t)j * D : (const __nv_bfloat16*)nullptr;
         });
         cp_async_wait_all();
         fence_proxy_async();
@@ -367,7 +374,11 @@ __global__ void __launch_bounds__(128)
             tmem_ld32(tS + c0, v);
             tmem_wait_ld();
             if (row < m)
-                for (int j = 0; j < 32 && c0 + j < nk; ++j) dst[c0 + j] = v[j];
+                for (int j = 0; j < 32 && c0 + j < nk; ++j) {
+                    const int u = t0 + c0 + j;
+                    const long long key = (long long)(u >> 4) * 16 * R + (u & 15);
+                    dst[c0 + j] = key < N ? v[j] : -INFINITY;  // slots past the last key rank last
+                }
         }
         fence_before_sync();
         __syncthreads();
@@ -1384,7 +1395,7 @@ struct ResTile {
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     k_expert_res(const __grid_constant__ CUtensorMap tmQp, const __nv_bfloat16* __restrict__ K,
                  const __nv_bfloat16* __restrict__ V, const int32_t* __restrict__ I, const int32_t* __restrict__ perm,
                  const int4* __restrict__ tiles, const int* __restrict__ tile_ctr, __nv_bfloat16* __restrict__ part,
@@ -1402,6 +1413,8 @@ __global__ void __launch_bounds__(192, 1)
     __shared__ ResTile tinfo[2];
     __shared__ int rowq[2][kT];
     __shared__ int keyrow[kT];
+    __shared__ float xmax[2][2][kT], xl[2][2][kT];  // [parity][half][row] exchange of the two softmax halves
+    __shared__ uint64_t xbar[2], ebar[2];          // exchange barriers (per chunk / per tile), one arrival per warp
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     volatile int* abort_v = &abort_flag;
@@ -1413,19 +1426,23 @@ __global__ void __launch_bounds__(192, 1)
     const int nloc = max(0, t_end - t_begin);
     if (nloc == 0) return;
     const int nex = (k + kT - 1) / kT;  // <= 2
-    if (warp == 5) tmem_alloc(&tmem_slot, 512);
+    if (warp == 9) tmem_alloc(&tmem_slot, 512);
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&q_full[i], 1);
-            mbar_init(&q_empty[i], 1 + 4);
+            mbar_init(&q_empty[i], 1 + 8);
             mbar_init(&kv_full[i], 32);
             mbar_init(&kv_free[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 4);
+            mbar_init(&p_full[i], 8);
             mbar_init(&o_full[i], 1);
-            mbar_init(&o_free[i], 4);
+            mbar_init(&o_free[i], 8);
         }
         mbar_init(&pv_done, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&xbar[i], 8);
+            mbar_init(&ebar[i], 8);
+        }
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -1435,7 +1452,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem = tmem_slot;
     constexpr int CPR = D / 8, RPI = 32 / CPR;  // 16-byte chunks per row, rows per warp instruction
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------- producer
         int cur_bh = -1, cur_e = -1, gen = 0;
         int armed_q[2] = {0, 0}, armed_kv[2] = {0, 0};
@@ -1503,7 +1520,7 @@ __global__ void __launch_bounds__(192, 1)
             }
         }
         cp_async_wait_all();  // nothing of ours may still be in flight when the CTA exits
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
             int g = 0, cur_gen = 0;
@@ -1550,6 +1567,8 @@ __global__ void __launch_bounds__(192, 1)
                     ptl = tl;
                     pfirst = c == 0;
                     plast = last;
+                    // the tile's epilogue waits on its last O += P V: issue it now
+                    if (last && !(ok = flush_pv())) break;
                 }
             }
             if (ok && pending) flush_pv();
@@ -1557,7 +1576,11 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
     } else {
         // -------------------------------------------- softmax + epilogue
-        const int r = threadIdx.x;
+        // two warpgroups share each row: wg 0 takes keys 0..63 of a chunk and
+        // output columns 0..D/2-1, wg 1 the other halves; the row max and the
+        // row sum are exchanged through shared memory (named barrier 1)
+        constexpr int DH = D / 2;
+        const int wg = warp >> 2, r = threadIdx.x & 127;
         int g = 0;
         for (int tl = 0; tl < nloc; ++tl) {
             const int qs = tl & 1, ob = tl & 1;
@@ -1566,40 +1589,48 @@ __global__ void __launch_bounds__(192, 1)
             const ResTile ti = tinfo[qs];
             const int pk = rowq[qs][r];
             const int q = pk >= 0 ? pk >> 3 : -1, slot = pk >= 0 ? pk & 7 : 0;
-            float mref = -INFINITY, l = 0.0f;
+            float mref = -INFINITY, l = 0.0f;  // l: this half's share of the row sum
             bool ok = true;
-            const uint32_t tO = lane_base(tmem) + kO0 + ob * 128;
+            const uint32_t tO = lane_base(tmem) + kO0 + ob * 128 + wg * DH;
             for (int c = 0; c < nex; ++c, ++g) {
                 const int sb = g & 1;
                 if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (g >> 1) & 1, status, abort_v))) { ok = false; break; }
                 if (threadIdx.x == 0) MITA_TRACE_EV(2, 21);
                 fence_after_sync();
                 const uint32_t tS = lane_base(tmem) + kS0 + sb * 128;
-                const int nval = q >= 0 ? min(kT, k - c * kT) : 0;
-                float v[kT];
-                tmem_ld32(tS, v);
-                tmem_ld32(tS + 32, v + 32);
-                tmem_ld32(tS + 64, v + 64);
-                tmem_ld32(tS + 96, v + 96);
+                const int nval = q >= 0 ? min(kT, k - c * kT) - 64 * wg : 0;  // valid columns of this half
+                float v[64];
+                tmem_ld32(tS + 64 * wg, v);
+                tmem_ld32(tS + 64 * wg + 32, v + 32);
                 tmem_wait_ld();
                 float mx = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < kT; ++j) mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
+                for (int j = 0; j < 64; ++j) mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
+                xmax[g & 1][wg][r] = mx;
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xbar[g & 1]);
+                // both halves have read S(g) and posted their max (bounded wait)
+                if (!__all_sync(0xffffffffu, ws_wait(&xbar[g & 1], (g >> 1) & 1, status, abort_v))) { ok = false; break; }
+                fence_after_sync();
+                mx = fmaxf(mx, xmax[g & 1][wg ^ 1][r]);
                 float mnew = mref, alpha = 1.0f;
                 if (mx > mref + 8.0f) {
                     mnew = mx;
                     alpha = ex2(mref - mnew);
                 }
                 float sum = 0.0f;
-                uint32_t pkd[64];
+                uint32_t pkd[32];
 #pragma unroll
-                for (int j = 0; j < kT; j += 2) {
+                for (int j = 0; j < 64; j += 2) {
                     const float e0 = ex2(fmaf(v[j], sl, -mnew)), e1 = ex2(fmaf(v[j + 1], sl, -mnew));
                     const float p0 = j < nval ? e0 : 0.0f, p1 = j + 1 < nval ? e1 : 0.0f;
                     sum += p0 + p1;
                     pkd[j >> 1] = pack_bf16(p0, p1);
                 }
-                tmem_store_p(tS, pkd);  // P over this row's scores
+                // P (bf16, two keys per column) over the scores: keys 64wg.. -> columns 32wg..
+                tmem_st32(tS + 32 * wg, reinterpret_cast<const float*>(pkd));
+                tmem_wait_st();
                 if (threadIdx.x == 0) MITA_TRACE_EV(2, 22);
                 l = l * alpha + sum;
                 mref = mnew;
@@ -1609,7 +1640,7 @@ __global__ void __launch_bounds__(192, 1)
                     fence_after_sync();
                     const float a = (c > 0) ? alpha : 1.0f;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
+                    for (int c0 = 0; c0 < DH; c0 += 32) {
                         float o[32];
                         tmem_ld32(tO + c0, o);
                         tmem_wait_ld();
@@ -1628,27 +1659,31 @@ __global__ void __launch_bounds__(192, 1)
             if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (tl >> 1) & 1, status, abort_v))) break;
             if (threadIdx.x == 0) MITA_TRACE_EV(2, 25);
             fence_after_sync();
-            float o[D];
+            float o[DH];
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(tO + c0, o + c0);
+            for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(tO + c0, o + c0);
             tmem_wait_ld();
+            xl[tl & 1][wg][r] = l;
             fence_before_sync();
             __syncwarp();
+            if (lane == 0) mbar_arrive(&ebar[tl & 1]);
+            if (!__all_sync(0xffffffffu, ws_wait(&ebar[tl & 1], (tl >> 1) & 1, status, abort_v))) break;
             if (lane == 0) {
                 mbar_arrive(&o_free[ob]);
                 mbar_arrive(&q_empty[qs]);
             }
-            if (q >= 0) {  // normalized partial of this (query, slot); the merge kernel combines them
+            if (q >= 0) {  // this half of the normalized partial of (query, slot)
+                const float lt = l + xl[tl & 1][wg ^ 1][r];
                 const size_t pr = ((size_t)ti.bh * N + q) * s + slot;
-                const float inv = 1.0f / l;
-                uint4* dst = reinterpret_cast<uint4*>(part + pr * D);
+                const float inv = 1.0f / lt;
+                uint4* dst = reinterpret_cast<uint4*>(part + pr * D + wg * DH);
 #pragma unroll
-                for (int u = 0; u < D / 8; ++u)
+                for (int u = 0; u < DH / 8; ++u)
                     dst[u] = make_uint4(pack_bf16(o[8 * u] * inv, o[8 * u + 1] * inv),
                                         pack_bf16(o[8 * u + 2] * inv, o[8 * u + 3] * inv),
                                         pack_bf16(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
                                         pack_bf16(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
-                lse[pr] = mref + __log2f(l);
+                if (wg == 0) lse[pr] = mref + __log2f(lt);
             }
             if (threadIdx.x == 0) MITA_TRACE_EV(2, 27);
         }
@@ -1656,7 +1691,7 @@ __global__ void __launch_bounds__(192, 1)
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (warp == 5) tmem_dealloc(tmem, 512);
+    if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
 // ------------------------------------------------------------------ host
@@ -1691,11 +1726,16 @@ TcPlan tc_plan(const Dims& D) {
     // sample stride ~ sqrt(N / 2k) balances the sample pass against the
     // candidates it lets through (about R * k per row); n_samp >= k always
     int R = (int)sqrt((double)D.N / (2.0 * D.k));
-    if (R > D.N / D.k) R = D.N / D.k;
     if (R > 32) R = 32;
     if (R < 1) R = 1;
+    // the sample must hold at least k real keys: runs of 16 every 16R keys
+    auto n_valid = [&](int r) {
+        const long long span = 16LL * r, full = D.N / span, rest = D.N - full * span;
+        return full * 16 + std::min<long long>(16, rest);
+    };
+    while (R > 1 && n_valid(R) < D.k) --R;
     p.R = R;
-    p.n_samp = (D.N + R - 1) / R;
+    p.n_samp = (int)(((long long)D.N + 16LL * R - 1) / (16LL * R) * 16);
     p.cand_cap = (long long)p.chunks_per_split * kT;
     p.resident = D.shared && p.m_pad == kT && D.k <= 2 * kT;
     return p;
@@ -1806,6 +1846,7 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
                                                                          P.m_pad, P.R, P.n_samp, cpc, status);
         if ((e = cudaGetLastError())) return e;
         count_launch();
+        prof_mark(st, "topk_threshold");
         if ((e = launch_sample_threshold(W.Ssamp, (long long)D.BH * D.m, P.n_samp, D.k, W.thr, st))) return e;
     }
     // landmark pass: top-k candidates and the shared-expert partials
@@ -1820,7 +1861,8 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
         count_launch();
     }
     prof_mark(st, "topk_select");
-    if ((e = launch_topk_cand(W.cand, W.ccount, P.splits, P.cand_cap, D.BH, D.m, P.m_pad, D.N, D.k, I, status, st)))
+    if ((e = launch_topk_cand(W.cand, W.ccount, P.splits, P.cand_cap, D.BH, D.m, P.m_pad, D.N, D.k,
+                              (long long)P.R * D.k, I, status, st)))
         return e;
     if (upto >= 2) {
         prof_mark(st, "vt_combine");
@@ -1858,7 +1900,7 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
             if ((e = tile_map(&mq, W.Qp, (long long)D.BH * D.N * D.s, DD))) return e;
             const int smem = 6 * tile + 1024;
             if ((e = set_smem(k_expert_res<DD>, smem))) return e;
-            k_expert_res<DD><<<num_sms(), 192, smem, st>>>(mq, kk, v, I, W.perm, W.tiles, W.tile_ctr, W.part, W.lse,
+            k_expert_res<DD><<<num_sms(), 320, smem, st>>>(mq, kk, v, I, W.perm, W.tiles, W.tile_ctr, W.part, W.lse,
                                                            D.N, D.m, D.k, D.s, sl, status);
             if ((e = cudaGetLastError())) return e;
             count_launch();
