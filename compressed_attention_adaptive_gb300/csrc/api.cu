@@ -149,7 +149,7 @@ static Work carve(const Dims& D, void* ws, size_t* bytes) {
         t.Ssamp = c.take<float>(BH * D.m * (size_t)P.n_samp);
         t.thr = c.take<float>(BH * D.m);
         t.cand = c.take<int2>(BH * P.m_pad * (size_t)P.splits * (size_t)P.cand_cap);
-        t.ccount = c.take<int>(BH * P.m_pad * (size_t)P.splits);
+        t.ccount = c.take<int>(BH * P.m_pad * (size_t)P.splits * 2);
         t.counts = c.take<int>(BH * D.m * 2);
         t.tile_ctr = c.take<int>(2);
         t.zero_begin = t.counts;

@@ -60,8 +60,8 @@ struct TcWork {
     float2* ML;                      // [BH][splits][m_pad]
     float* Ssamp;                    // [BH][m][n_samp] sample scores
     float* thr;                      // [BH][m] candidate thresholds
-    int2* cand;                      // [BH][m_pad][splits][cand_cap] (score, key) records
-    int* ccount;                     // [BH][m_pad][splits]
+    int2* cand;                      // [BH][m_pad][splits][2][cand_cap / 2] (score, key) records
+    int* ccount;                     // [BH][m_pad][splits][2]
     int* counts;                     // [BH][m][2]
     int* tile_ctr;                   // [2]: tiles written, tiles taken
     void* zero_begin;                // counts .. tile_ctr, cleared each call

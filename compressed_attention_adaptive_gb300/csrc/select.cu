@@ -189,11 +189,16 @@ __global__ void __launch_bounds__(512) k_topk_cand(const int2* __restrict__ cand
     const int* cnts = ccount + rrow * splits;
     const int2* base = cand + rrow * splits * cap;
     for (int w = threadIdx.x; w < nwords; w += blockDim.x) bits[w] = 0u;
+    // region counts: read in parallel (up to 64 staged), then prefix offsets
+    __shared__ int sh_cnt[64];
+    for (int sp = threadIdx.x; sp < 64; sp += blockDim.x) sh_cnt[sp] = sp < splits ? cnts[sp] : 0;
+    __syncthreads();
     if (threadIdx.x == 0) {
         int tot = 0;
         for (int sp = 0; sp < splits; ++sp) {
+            const int c = sp < 64 ? sh_cnt[sp] : cnts[sp];
             if (sp < 64) sh_off[sp] = tot;
-            tot += cnts[sp];
+            tot += c;
         }
         sh_total = tot;
     }
@@ -208,7 +213,7 @@ __global__ void __launch_bounds__(512) k_topk_cand(const int2* __restrict__ cand
     CandSrc cs{nullptr, nullptr, 0, base, cnts, splits, cap};
     if (total <= stage_cap && splits <= 64) {  // one read of the records, the passes run in shared memory
         for (int sp = 0; sp < splits; ++sp) {
-            const int c = cnts[sp], o = sh_off[sp];
+            const int c = sh_cnt[sp], o = sh_off[sp];
             const int2* b = base + sp * cap;
             for (int t = threadIdx.x; t < c; t += blockDim.x) {
                 const int2 r = b[t];

@@ -57,6 +57,23 @@ __device__ __forceinline__ bool sync_on_mma(uint64_t* bar, uint32_t& phase, int*
     return !bad;
 }
 
+// Bounded wait used by the warp-specialized kernels: gives up when another
+// role has set the abort flag, or after about a second (then sets the device
+// status and the abort flag itself).
+__device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > (2LL << 30)) {
+            set_status(status, kStTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
 // Issues S = A * B^T over the head dim D (K-major A and B tiles of 128 rows).
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t sA, uint32_t sB, bool accumulate_first) {
@@ -81,15 +98,6 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t sP, uint32_t sV, 
     }
 }
 
-// Where the landmark pass sends the raw scores of a row that pass the
-// row's threshold: (score, key index) records appended at cand[n++].
-struct CandOut {
-    int2* cand;  // nullptr: no emission
-    float thr;
-    int j0;      // key index of column 0 of the chunk
-    int n;
-};
-
 // Issues O (+)= P * V with P (128 x 128 bf16) in TMEM at column tP (eight
 // columns per 16 keys) and V an MN-major 128 keys x D tile in shared memory.
 template <int D>
@@ -106,70 +114,6 @@ __device__ __forceinline__ void tmem_store_p(uint32_t tP, const uint32_t (&pk)[6
     tmem_st32(tP, reinterpret_cast<const float*>(pk));
     tmem_st32(tP + 32, reinterpret_cast<const float*>(pk + 32));
     tmem_wait_st();
-}
-
-// Online softmax of this thread's row of one chunk of scores held in TMEM.
-// nk keys are valid; sl = scale * log2(e). The reference max moves only when
-// the chunk max exceeds it by more than 8 (probabilities stay <= 2^8), and
-// then O (TMEM) is rescaled. Raw scores >= co.thr are emitted when co.cand.
-template <int D>
-__device__ __forceinline__ void chunk_softmax(uint32_t tS, uint32_t tO, uint8_t* sP, int nk, bool row_ok, float sl,
-                                              bool first, float& mref, float& l, CandOut& co) {
-    const int r = threadIdx.x;
-    float mx = -INFINITY;
-#pragma unroll 1
-    for (int c0 = 0; c0 < kT; c0 += 32) {
-        float v[32];
-        tmem_ld32(tS + c0, v);
-        tmem_wait_ld();
-        if (co.cand && row_ok) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (c0 + j < nk && v[j] >= co.thr) co.cand[co.n++] = make_int2(__float_as_int(v[j]), co.j0 + c0 + j);
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (row_ok && c0 + j < nk) mx = fmaxf(mx, v[j] * sl);
-    }
-    float mnew = mref, alpha = 1.0f;
-    if (mx > mref + 8.0f) {
-        mnew = mx;
-        alpha = ex2(mref - mnew);
-    }
-    float sum = 0.0f;
-#pragma unroll 1
-    for (int c0 = 0; c0 < kT; c0 += 32) {
-        float v[32];
-        tmem_ld32(tS + c0, v);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-            const float p0 = (row_ok && c0 + j < nk) ? ex2(fmaf(v[j], sl, -mnew)) : 0.0f;
-            const float p1 = (row_ok && c0 + j + 1 < nk) ? ex2(fmaf(v[j + 1], sl, -mnew)) : 0.0f;
-            sum += p0 + p1;
-            pk[j >> 1] = pack_bf16(p0, p1);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(sP + sw_off(r, (c0 >> 3) + q, kT)) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-    }
-    l = l * alpha + sum;
-    mref = mnew;
-    const bool resc = !first && alpha != 1.0f;
-    if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            float o[32];
-            tmem_ld32(tO + c0, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] *= alpha;
-            tmem_st32(tO + c0, o);
-        }
-        tmem_wait_st();
-    }
 }
 
 // Copies an R-row operand tile (R a multiple of 8): row t comes from
@@ -209,110 +153,6 @@ __device__ __forceinline__ void top_insert(uint32_t (&bu)[SMAX], int (&bi)[SMAX]
 }
 
 }  // namespace
-
-// ------------------------------------------------------------------------
-// Landmark pass: per (landmark tile, key split, head). S = Qhi K^T + Qlo K^T
-// (the bf16 split of fp32 Qt keeps the ranking scores at fp32 accuracy);
-// every score at or above its row's threshold is recorded as a top-k
-// candidate, and an online-softmax partial of Vt over the split is written.
-template <int D>
-__global__ void __launch_bounds__(128, 1)
-    k_landmark_tc(const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
-                  const __nv_bfloat16* __restrict__ Qhi, const __nv_bfloat16* __restrict__ Qlo,
-                  const float* __restrict__ thr, int2* __restrict__ cand, int* __restrict__ ccount,
-                  float* __restrict__ Opart, float2* __restrict__ ML, int N, int m, int m_pad,
-                  int splits, int chunks_per_split, float sl, int* __restrict__ status) {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar;
-    __shared__ uint32_t tmem_slot;
-    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    constexpr int TILE = kT * D * 2;
-    constexpr int kKP = kp_bytes<D>();
-    uint8_t* sHi = sm;
-    uint8_t* sLo = sm + TILE;
-    uint8_t* sK = sm + 2 * TILE;  // also the P tile (128 x 128 bf16) once S is in TMEM
-    uint8_t* sV = sK + kKP;
-    const int mt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z, r = threadIdx.x;
-
-    if (r < 32) tmem_alloc(&tmem_slot, 256);
-    if (r == 0) {
-        mbar_init(&bar, 1);
-        fence_mbar_init();
-    }
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    const uint32_t tmem = tmem_slot;
-    const uint32_t tS = lane_base(tmem), tO = lane_base(tmem) + 128;
-    uint32_t phase = 0;
-
-    const size_t qrow0 = (size_t)bh * m_pad + (size_t)mt * kT;
-    load_tile<D>(smem_u32(sHi), [&](int t) { return Qhi + (qrow0 + (t < 0 ? 0 : t)) * D; });
-    load_tile<D>(smem_u32(sLo), [&](int t) { return Qlo + (qrow0 + (t < 0 ? 0 : t)) * D; });
-
-    const int row = mt * kT + r;
-    const bool row_ok = row < m;
-    const int j_begin = sp * chunks_per_split * kT;
-    const int j_end = min(N, j_begin + chunks_per_split * kT);
-    const __nv_bfloat16* Kb = K + (size_t)bh * N * D;
-    const __nv_bfloat16* Vb = V + (size_t)bh * N * D;
-    float mref = -INFINITY, l = 0.0f;
-    bool ok = true;
-    int c = 0;
-    const size_t crow = ((size_t)bh * m_pad + row) * splits + sp;  // this row's record region of this split
-    CandOut co;
-    co.cand = row_ok ? cand + crow * (size_t)chunks_per_split * kT : nullptr;
-    co.thr = row_ok ? thr[(size_t)bh * m + row] : 0.0f;
-    co.n = 0;
-    for (int j0 = j_begin; j0 < j_end; j0 += kT, ++c) {
-        const int nk = min(kT, j_end - j0);
-        load_tile<D>(smem_u32(sK), [&](int t) { return (t >= 0 && t < nk) ? Kb + (size_t)(j0 + t) * D : (t < 0 ? Kb : nullptr); });
-        load_tile<D>(smem_u32(sV), [&](int t) { return (t >= 0 && t < nk) ? Vb + (size_t)(j0 + t) * D : (t < 0 ? Vb : nullptr); });
-        cp_async_wait_all();
-        fence_proxy_async();
-        __syncthreads();
-        if (r == 0) {
-            fence_after_sync();
-            issue_qk<D>(tS, smem_u32(sHi), smem_u32(sK), false);
-            issue_qk<D>(tS, smem_u32(sLo), smem_u32(sK), true);
-            mma_commit(&bar);
-        }
-        if (!(ok = sync_on_mma(&bar, phase, status))) break;
-        co.j0 = j0;
-        chunk_softmax<D>(tS, tO, sK, nk, row_ok, sl, c == 0, mref, l, co);
-        fence_proxy_async();
-        fence_before_sync();
-        __syncthreads();
-        if (r == 0) {
-            fence_after_sync();
-            issue_pv<D>(tO, smem_u32(sK), smem_u32(sV), c > 0);
-            mma_commit(&bar);
-        }
-        if (!(ok = sync_on_mma(&bar, phase, status))) break;
-    }
-    if (ok) {
-        const size_t orow = ((size_t)bh * splits + sp) * m_pad + row;
-        if (c == 0) {  // empty split (cannot happen with the host's split sizing)
-            for (int c0 = 0; c0 < D; ++c0) Opart[orow * D + c0] = 0.0f;
-        } else {
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float o[32];
-                tmem_ld32(tO + c0, o);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4*>(Opart + orow * D + c0 + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-            }
-        }
-        ML[orow] = make_float2(mref, l);
-        ccount[crow] = co.n;
-    }
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    if (r < 32) tmem_dealloc(tmem, 256);
-}
 
 // Sample pass of the top-k selection: raw scores of each landmark row against
 // a sample of the keys (runs of 16 consecutive keys, one run every 16R keys;
@@ -387,6 +227,220 @@ __global__ void __launch_bounds__(128)
     __syncthreads();
     fence_after_sync();
     if (r < 32) tmem_dealloc(tmem, 128);
+}
+
+// Landmark pass, warp-specialized: per (landmark tile, key split, head).
+//   warps 0-7  two softmax warpgroups, one per half of each 128-key chunk
+//              (thread <-> TMEM lane = landmark row); they emit the top-k
+//              candidates of their columns and share the row max / sum
+//   warp 8     producer: the landmark tile (hi, lo) once, then TMA bulk
+//              loads of consecutive K and V chunks into an NS-stage ring
+//   warp 9     MMA issuer: S = Qhi K^T + Qlo K^T (bf16 split of fp32 Qt) into
+//              one of two TMEM buffers, O += P V with P written over S in TMEM
+// Candidate records of column half w go to region (row, split, w), whose
+// capacity is that half's key count (chunks_per_split * 64).
+template <int D, int NS>
+__global__ void __launch_bounds__(320, 1)
+    k_landmark_ws(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __nv_bfloat16* __restrict__ Qhi, const __nv_bfloat16* __restrict__ Qlo,
+                  const float* __restrict__ thr, int2* __restrict__ cand, int* __restrict__ ccount,
+                  float* __restrict__ Opart, float2* __restrict__ ML, int N, int m, int m_pad, int splits,
+                  int chunks_per_split, float sl, int* __restrict__ status) {
+    constexpr int TILE = kT * D * 2;
+    constexpr int DH = D / 2;
+    constexpr uint32_t kS0 = 0, kO = 256;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sHi = sm;
+    uint8_t* sLo = sm + TILE;
+    uint8_t* sK = sm + 2 * TILE;   // NS stages
+    uint8_t* sV = sK + NS * TILE;  // NS stages
+    __shared__ uint64_t kv_full[NS], kv_empty[NS], s_full[2], p_full[2], xbar[2];
+    __shared__ uint64_t pv_done, o_full, q_bar, ebar;
+    __shared__ float xmax[2][2][kT], xl[2][kT];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    volatile int* abort_v = &abort_flag;
+    const int mt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j_begin = sp * chunks_per_split * kT;
+    const int j_end = min(N, j_begin + chunks_per_split * kT);
+    const int nc = (j_end - j_begin + kT - 1) / kT;  // >= 1 by the host's split sizing
+    if (warp == 9) tmem_alloc(&tmem_slot, 512);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 8);
+            mbar_init(&xbar[i], 8);
+        }
+        mbar_init(&pv_done, 1);
+        mbar_init(&o_full, 1);
+        mbar_init(&q_bar, 32);
+        mbar_init(&ebar, 8);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    if (warp == 8) {
+        // ------------------------------------------------------- producer
+        {
+            constexpr int CPR = D / 8, RPI = 32 / CPR;
+            const int cc = lane % CPR;
+            const size_t y0 = (size_t)bh * m_pad + (size_t)mt * kT;
+            for (int r0 = 0; r0 < kT; r0 += RPI) {
+                const int r = r0 + lane / CPR;
+                cp_async16(smem_u32(sHi) + sw_off(r, cc, kT), Qhi + (y0 + r) * D + cc * 8, true);
+                cp_async16(smem_u32(sLo) + sw_off(r, cc, kT), Qlo + (y0 + r) * D + cc * 8, true);
+            }
+            cp_async_arrive(&q_bar);
+        }
+        if (lane == 0) {
+            for (int c = 0; c < nc; ++c) {
+                const int st = c % NS, use = c / NS;
+                if (!ws_wait(&kv_empty[st], (use & 1) ^ 1, status, abort_v)) break;
+                mbar_expect_tx(&kv_full[st], 2 * TILE);
+                const int y = bh * N + j_begin + c * kT;  // rows past the split are masked, past the end read 0
+#pragma unroll
+                for (int cb = 0; cb < D / 64; ++cb) {
+                    tma_load_2d(smem_u32(sK + st * TILE) + cb * kT * 128, &tmK, cb * 64, y, &kv_full[st]);
+                    tma_load_2d(smem_u32(sV + st * TILE) + cb * kT * 128, &tmV, cb * 64, y, &kv_full[st]);
+                }
+            }
+        }
+        __syncwarp();
+        cp_async_wait_all();
+    } else if (warp == 9) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = ws_wait(&q_bar, 0, status, abort_v);
+            fence_proxy_async();  // the landmark tiles came through cp.async (generic proxy)
+            auto flush_pv = [&](int h) -> bool {
+                if (!ws_wait(&p_full[h & 1], (h >> 1) & 1, status, abort_v)) return false;
+                fence_after_sync();
+                issue_pv_ts<D>(tmem + kO, tmem + kS0 + (h & 1) * 128, smem_u32(sV + (h % NS) * TILE), h > 0);
+                mma_commit(&pv_done);
+                mma_commit(&kv_empty[h % NS]);
+                if (h == nc - 1) mma_commit(&o_full);
+                return true;
+            };
+            for (int c = 0; c < nc && ok; ++c) {
+                const int st = c % NS, sb = c & 1;
+                if (!(ok = ws_wait(&kv_full[st], (c / NS) & 1, status, abort_v))) break;
+                fence_after_sync();
+                issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sHi), smem_u32(sK + st * TILE), false);
+                issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sLo), smem_u32(sK + st * TILE), true);
+                mma_commit(&s_full[sb]);
+                if (c > 0 && !(ok = flush_pv(c - 1))) break;
+            }
+            if (ok) flush_pv(nc - 1);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------- softmax + epilogue
+        const int wg = warp >> 2, r = threadIdx.x & 127;
+        const int row = mt * kT + r;
+        const bool row_ok = row < m;
+        const float th = row_ok ? thr[(size_t)bh * m + row] : 0.0f;
+        const long long capw = (long long)chunks_per_split * 64;
+        const size_t region = (((size_t)bh * m_pad + row) * splits + sp) * 2 + wg;
+        int2* cw = cand + region * capw;
+        int ncand = 0;
+        float mref = -INFINITY, l = 0.0f;
+        bool ok = true;
+        const uint32_t tO = lane_base(tmem) + kO + wg * DH;
+        for (int c = 0; c < nc; ++c) {
+            const int sb = c & 1, j0 = j_begin + c * kT;
+            if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (c >> 1) & 1, status, abort_v))) { ok = false; break; }
+            fence_after_sync();
+            const uint32_t tS = lane_base(tmem) + kS0 + sb * 128;
+            const int nval = row_ok ? min(kT, j_end - j0) - 64 * wg : 0;
+            float v[64];
+            tmem_ld32(tS + 64 * wg, v);
+            tmem_ld32(tS + 64 * wg + 32, v + 32);
+            tmem_wait_ld();
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                if (j < nval && v[j] >= th) cw[ncand++] = make_int2(__float_as_int(v[j]), j0 + 64 * wg + j);
+                mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
+            }
+            xmax[c & 1][wg][r] = mx;
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xbar[c & 1]);
+            if (!__all_sync(0xffffffffu, ws_wait(&xbar[c & 1], (c >> 1) & 1, status, abort_v))) { ok = false; break; }
+            fence_after_sync();
+            mx = fmaxf(mx, xmax[c & 1][wg ^ 1][r]);
+            float mnew = mref, alpha = 1.0f;
+            if (mx > mref + 8.0f) {
+                mnew = mx;
+                alpha = ex2(mref - mnew);
+            }
+            float sum = 0.0f;
+            uint32_t pkd[32];
+#pragma unroll
+            for (int j = 0; j < 64; j += 2) {
+                const float e0 = ex2(fmaf(v[j], sl, -mnew)), e1 = ex2(fmaf(v[j + 1], sl, -mnew));
+                const float p0 = j < nval ? e0 : 0.0f, p1 = j + 1 < nval ? e1 : 0.0f;
+                sum += p0 + p1;
+                pkd[j >> 1] = pack_bf16(p0, p1);
+            }
+            tmem_st32(tS + 32 * wg, reinterpret_cast<const float*>(pkd));
+            tmem_wait_st();
+            l = l * alpha + sum;
+            mref = mnew;
+            if (__any_sync(0xffffffffu, c > 0 && alpha != 1.0f)) {
+                // S(c) done implies PV(c-2) done: this wait can only see PV(c-1)'s phase
+                if (!__all_sync(0xffffffffu, ws_wait(&pv_done, (c - 1) & 1, status, abort_v))) { ok = false; break; }
+                fence_after_sync();
+                const float a = (c > 0) ? alpha : 1.0f;
+#pragma unroll 1
+                for (int c0 = 0; c0 < DH; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(tO + c0, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] *= a;
+                    tmem_st32(tO + c0, o);
+                }
+                tmem_wait_st();
+            }
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[c & 1]);
+        }
+        if (ok && __all_sync(0xffffffffu, ws_wait(&o_full, 0, status, abort_v))) {
+            fence_after_sync();
+            float o[DH];
+#pragma unroll
+            for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(tO + c0, o + c0);
+            tmem_wait_ld();
+            xl[wg][r] = l;
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ebar);
+            if (__all_sync(0xffffffffu, ws_wait(&ebar, 0, status, abort_v))) {
+                const float lt = l + xl[wg ^ 1][r];
+                const size_t orow = ((size_t)bh * splits + sp) * m_pad + row;
+                float* od = Opart + orow * D + wg * DH;
+#pragma unroll
+                for (int j = 0; j < DH; j += 4) *reinterpret_cast<float4*>(od + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+                if (wg == 0) ML[orow] = make_float2(mref, row_ok ? lt : 0.0f);
+                ccount[region] = ncand;
+            }
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
 // Merges the per-split partials: Vt = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
@@ -1010,20 +1064,6 @@ struct WsMeta {  // what the deferred O += P V of a chunk needs
     int st, ob, tseq;
     bool first, last;
 };
-
-__device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort_flag) return false;
-        if (clock64() - t0 > (2LL << 30)) {
-            set_status(status, kStTimeout);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-    return true;
-}
 
 template <int D>
 __global__ void __launch_bounds__(192, 1)
@@ -1852,16 +1892,21 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
     // landmark pass: top-k candidates and the shared-expert partials
     prof_mark(st, "landmark");
     {
-        const int smem = std::max(3 * tile + kp_bytes<DD>(), 100 * 1024) + 1024;
-        if ((e = set_smem(k_landmark_tc<DD>, smem))) return e;
+        alignas(64) CUtensorMap mk, mv;
+        const long long rows = (long long)D.BH * D.N;
+        if ((e = tile_map(&mk, kk, rows, DD)) || (e = tile_map(&mv, v, rows, DD))) return e;
+        constexpr int NS = DD == 64 ? 4 : 2;
+        const int smem = (2 + 2 * NS) * tile + 1024;
+        if ((e = set_smem(k_landmark_ws<DD, NS>, smem))) return e;
         dim3 grid(P.m_tiles, P.splits, D.BH);
-        k_landmark_tc<DD><<<grid, 128, smem, st>>>(kk, v, W.Qhi, W.Qlo, W.thr, W.cand, W.ccount, W.Opart, W.ML, D.N,
-                                                  D.m, P.m_pad, P.splits, P.chunks_per_split, sl, status);
+        k_landmark_ws<DD, NS><<<grid, 320, smem, st>>>(mk, mv, W.Qhi, W.Qlo, W.thr, W.cand, W.ccount, W.Opart, W.ML,
+                                                      D.N, D.m, P.m_pad, P.splits, P.chunks_per_split, sl, status);
         if ((e = cudaGetLastError())) return e;
         count_launch();
     }
     prof_mark(st, "topk_select");
-    if ((e = launch_topk_cand(W.cand, W.ccount, P.splits, P.cand_cap, D.BH, D.m, P.m_pad, D.N, D.k,
+    // two record regions (column halves) per (row, split)
+    if ((e = launch_topk_cand(W.cand, W.ccount, 2 * P.splits, P.cand_cap / 2, D.BH, D.m, P.m_pad, D.N, D.k,
                               (long long)P.R * D.k, I, status, st)))
         return e;
     if (upto >= 2) {
