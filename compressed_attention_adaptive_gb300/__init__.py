@@ -86,6 +86,8 @@ def lib():
         L.mita_last_error.argtypes = []
         L.mita_last_error.restype = ctypes.c_char_p
         L.mita_uses_tensor_cores.argtypes = [P]
+        L.mita_forward_static.argtypes = [P, vp, vp, vp, vp, ip, vp]
+        L.mita_forward_static.restype = ctypes.c_int
         L.mita_launch_count.argtypes = []
         L.mita_launch_count.restype = ctypes.c_longlong
         L.mita_profile_begin.argtypes = [ctypes.c_int]
@@ -167,6 +169,14 @@ def mita_select(p: Params, Q, K, idx, route, ws, stream=None):
 def mita_forward(p: Params, Q, K, V, O, ws, idx_out=None, route_out=None, Vt_out=None, stream=None):
     _check(lib().mita_forward(ctypes.byref(p.c()), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(idx_out),
                               _ptr(route_out), _ptr(Vt_out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def mita_forward_static(p: Params, Q, K, V, O, status_out=None, stream=None):
+    """The forward pass on the library's static device workspace (nothing is
+    allocated): for callers that cannot allocate device memory. status_out is
+    an optional int32 device tensor receiving the device status word."""
+    _check(lib().mita_forward_static(ctypes.byref(p.c()), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(status_out),
+                                     _stream(stream)))
 
 
 def mita_forward_host(p: Params, Q, K, V, O, dev, stream=None):

@@ -228,6 +228,20 @@ static mita_status run(const mita_params* p, const void* Q, const void* K, const
     return MITA_OK;
 }
 
+// For other translation units of the library: argument check, error report
+// and the whole forward pass on a given workspace.
+mita_status validate(const mita_params* p) {
+    Dims D;
+    return resolve(p, &D);
+}
+
+mita_status report_error(mita_status st, const char* msg) { return fail(st, "%s", msg); }
+
+mita_status forward_on_workspace(const mita_params* p, const void* Q, const void* K, const void* V, void* O,
+                                 void* ws, size_t ws_bytes, void* stream) {
+    return run(p, Q, K, V, O, nullptr, nullptr, nullptr, nullptr, ws, ws_bytes, stream, 2);
+}
+
 }  // namespace mita
 
 using namespace mita;

@@ -16,6 +16,15 @@ constexpr int kMaxS = 8;  // routed experts per query the kernels support
 void prof_mark(cudaStream_t st, const char* phase);
 void count_launch(int n = 1);
 
+// api.cu (for the static-workspace entry point)
+}  // namespace mita
+#include "../../include/mita.h"
+namespace mita {
+mita_status validate(const mita_params* p);
+mita_status report_error(mita_status st, const char* msg);
+mita_status forward_on_workspace(const mita_params* p, const void* Q, const void* K, const void* V, void* O,
+                                 void* ws, size_t ws_bytes, void* stream);
+
 // simt.cu
 cudaError_t launch_pool(const Dims& D, const void* Q, float* Qt, __nv_bfloat16* hi, __nv_bfloat16* lo, int m_pad,
                         int* status, cudaStream_t st);

@@ -127,6 +127,33 @@ const char* mita_last_error(void);
 /* 1 if `p` runs on the tcgen05 tensor-core path, 0 if on CUDA cores, -1 if invalid. */
 int mita_uses_tensor_cores(const mita_params* p);
 
+/* ---- forward pass without device allocation --------------------------------
+ * Not part of the method (the summaries have no counterpart): an interface
+ * for callers that cannot allocate device memory. Some code may not call
+ * cudaMalloc at all: it can synchronize the whole device, another framework
+ * may own all device memory through its own pool, or the caller is a plugin
+ * that only receives the tensors it works on. mita_forward_static() is
+ * mita_forward() with its workspace in a library-owned static device array of
+ * MITA_STATIC_WORKSPACE_BYTES, so the caller passes only Q, K, V and O.
+ *   - Problems whose mita_workspace_size() exceeds the static area are
+ *     rejected with MITA_ERR_UNSUPPORTED; nothing is enqueued.
+ *   - The call allocates nothing (no cudaMalloc, no allocating library call).
+ *     Every GPU on which the library is loaded holds the static area until the
+ *     process exits.
+ *   - The first call on a device looks up the area's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture. `stream` must belong to the current device.
+ *   - All calls share the one area, which keeps the last call's contents; the
+ *     pass clears what must start at zero itself. Calls whose work overlaps on
+ *     the GPU (different streams, or concurrent host threads) race on the area
+ *     and must be serialized by the caller.
+ *   - status_out (optional, device int32) receives the call's device status
+ *     word (MITA_OK or MITA_ERR_TIMEOUT / MITA_ERR_BOUNDS) once the stream
+ *     reaches it. */
+#define MITA_STATIC_WORKSPACE_BYTES (64u << 20)
+mita_status mita_forward_static(const mita_params* p, const void* Q, const void* K, const void* V, void* O,
+                                int32_t* status_out, void* stream);
+
 /* ---- measurement hooks (not part of the method) ---------------------------
  * Number of kernels this library has launched in the process so far. */
 long long mita_launch_count(void);
