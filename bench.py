@@ -29,9 +29,10 @@ sys.path.insert(0, ROOT)
 METRIC = "MiTA fwd query-tokens/sec·head and % roofline at N=32k bf16, 1×GB300"
 UNIT = "query-tokens/s·head"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# dram__bytes_read.sum + dram__bytes_write.sum of one expert-attention launch on
-# the 32k long-context workload (None until a capture of the current kernel).
-EXPERT_TRAFFIC_BYTES = None
+# dram__bytes_read.sum + dram__bytes_write.sum of one expert-attention launch
+# (k_expert_res) on the 32k long-context workload: a 6-head capture (195 MB)
+# scaled by 32 / 6 heads (profiles/k_expert_res_longctx_6heads.md).
+EXPERT_TRAFFIC_BYTES = 1.04e9
 
 
 def peaks():
@@ -241,9 +242,12 @@ def main():
     dom = "expert" if "expert" in phase_ms else max(phase_ms, key=phase_ms.get)
     dom_ms = phase_ms[dom]
     achieved = expert_F / (dom_ms * 1e-3) / 1e12
-    roof = {"kernel": "k_expert_tc (expert attention + merge)" if dom == "expert" else dom,
+    kname = "k_expert_res (expert attention)" if "merge" in phase_ms else "k_expert_ws (expert attention + merge)"
+    roof = {"kernel": kname if dom == "expert" else dom,
             "bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
-            "frac": achieved / tensor_peak, "traffic": EXPERT_TRAFFIC_BYTES,
+            "frac": achieved / tensor_peak,
+            "traffic": EXPERT_TRAFFIC_BYTES if (dom == "expert" and w.name == "longctx_n32k" and "merge" in phase_ms)
+            else None,
             "peak_source": "%s bf16 sustained (MEASURED_PEAKS.json)" % pk_src,
             "algorithmic_flops_per_launch": expert_F, "avg_launch_ms": dom_ms}
 
