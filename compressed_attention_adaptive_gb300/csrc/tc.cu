@@ -213,12 +213,21 @@ __global__ void __launch_bounds__(128)
             float v[32];
             tmem_ld32(tS + c0, v);
             tmem_wait_ld();
-            if (row < m)
-                for (int j = 0; j < 32 && c0 + j < nk; ++j) {
-                    const int u = t0 + c0 + j;
-                    const long long key = (long long)(u >> 4) * 16 * R + (u & 15);
-                    dst[c0 + j] = key < N ? v[j] : -INFINITY;  // slots past the last key rank last
+            if (row < m) {
+                const int u0 = t0 + c0;
+                const long long last = (long long)((u0 + 31) >> 4) * 16 * R + ((u0 + 31) & 15);
+                if (c0 + 32 <= nk && last < N) {  // all 32 slots real keys: eight 16-byte stores
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                } else {
+                    for (int j = 0; j < 32 && c0 + j < nk; ++j) {
+                        const int u = u0 + j;
+                        const long long key = (long long)(u >> 4) * 16 * R + (u & 15);
+                        dst[c0 + j] = key < N ? v[j] : -INFINITY;  // slots past the last key rank last
+                    }
                 }
+            }
         }
         fence_before_sync();
         __syncthreads();
@@ -606,169 +615,252 @@ __global__ void __launch_bounds__(128, 1)
     if (r < 32) tmem_dealloc(tmem, tmem_cols);
 }
 
-// Variant for m_pad == 128 that also computes each query's shared-slot
-// partial: the routing scores R = Q Qt^T are the shared slots' logits (scaled),
-// so the same row gives the routes and softmax(scale R) Vt, written as a
-// normalized bf16 partial output with its log2-sum-exp. Qt (hi, lo) and Vt of
-// the current head stay in shared memory; the probabilities overwrite the
-// row's scores in TMEM and feed the P Vt MMA from there.
-template <int D, int SMAX>
-__global__ void __launch_bounds__(128, 1)
-    k_route_shared_tc(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Qhi,
-                      const __nv_bfloat16* __restrict__ Qlo, const __nv_bfloat16* __restrict__ Vtb, int N, int m,
-                      int s, int tiles_per_head, int total_tiles, float sl, int32_t* __restrict__ E,
-                      int* __restrict__ cnt, __nv_bfloat16* __restrict__ sh_part, float* __restrict__ sh_lse,
-                      int* __restrict__ status) {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar_r, bar_o;  // R MMAs / the P Vt MMA
-    __shared__ uint32_t tmem_slot;
-    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+// Routing + shared slots, warp-specialized and persistent (m_pad == 128):
+//   warps 0-7  two warpgroups, one per half of the 128 landmark columns: each
+//              keeps the s best landmarks of its half and the halves merge in
+//              a fixed order (ties to the lower landmark index); the softmax
+//              over the shared logits shares its row max / sum the same way
+//   warp 8     producer: TMA loads of consecutive 128-query tiles (NSQ-stage
+//              ring); the head's Qt (hi, lo) and Vt when the head changes
+//   warp 9     MMA issuer: R = Q Qhi^T + Q Qlo^T into one of two TMEM
+//              buffers; P Vt (P over R in TMEM) into one of two outputs
+template <int D, int SMAX, int NSQ>
+__global__ void __launch_bounds__(320, 1)
+    k_route_ws(const __grid_constant__ CUtensorMap tmQ, const __nv_bfloat16* __restrict__ Qhi,
+               const __nv_bfloat16* __restrict__ Qlo, const __nv_bfloat16* __restrict__ Vtb, int N, int m, int s,
+               int tiles_per_head, int total_tiles, float sl, int32_t* __restrict__ E, int* __restrict__ cnt,
+               __nv_bfloat16* __restrict__ sh_part, float* __restrict__ sh_lse, int* __restrict__ status) {
     constexpr int TILE = kT * D * 2;
+    constexpr int DH = D / 2;
+    constexpr uint32_t kR0 = 0, kO0 = 256;  // TMEM: R/P buffers 0 / 128, outputs 256 / 256 + D
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sHi = sm;
     uint8_t* sLo = sm + TILE;
     uint8_t* sVt = sm + 2 * TILE;
-    uint8_t* sQb[2] = {sm + 3 * TILE, sm + 4 * TILE};
-    constexpr uint32_t kO = 256;  // TMEM: R buffers at columns 0 / 128, the shared output at 256
-    const int r = threadIdx.x;
+    uint8_t* sQ = sm + 3 * TILE;  // NSQ stages
+    __shared__ uint64_t q_full[NSQ], q_empty[NSQ], r_full[2], p_full[2], o_full[2], o_free[2];
+    __shared__ uint64_t lm_full, lm_free, xbar, ebar;  // lm_free: the MMA warp is done with a head's landmarks
+    __shared__ int qgen[NSQ];  // landmark load each query tile uses (1-based)
+    __shared__ float xmax[2][kT], xl[2][kT];
+    __shared__ uint32_t xkey[2][kT][SMAX];
+    __shared__ int xidx[2][kT][SMAX];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    volatile int* abort_v = &abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per = (total_tiles + gridDim.x - 1) / gridDim.x;
     const int t_begin = blockIdx.x * per, t_end = min(total_tiles, t_begin + per);
-    if (t_begin >= t_end) return;
-    if (r < 32) tmem_alloc(&tmem_slot, 512);
-    if (r == 0) {
-        mbar_init(&bar_r, 1);
-        mbar_init(&bar_o, 1);
+    const int nloc = max(0, t_end - t_begin);
+    if (nloc == 0) return;
+    if (warp == 9) tmem_alloc(&tmem_slot, 512);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSQ; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&r_full[i], 1);
+            mbar_init(&p_full[i], 8);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_free[i], 8);
+        }
+        mbar_init(&lm_full, 32);
+        mbar_init(&lm_free, 1);
+        mbar_init(&xbar, 8);
+        mbar_init(&ebar, 8);
+        abort_flag = 0;
         fence_mbar_init();
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = tmem_slot;
-    uint32_t phase_r = 0, phase_o = 0;
-
-    auto load_q = [&](int t, int b) {
-        const int bh = t / tiles_per_head, q0 = (t % tiles_per_head) * kT;
-        const __nv_bfloat16* Qb = Q + (size_t)bh * N * D;
-        load_tile<D>(smem_u32(sQb[b]), [&](int i) {
-            return i < 0 ? Qb : (q0 + i < N ? Qb + (size_t)(q0 + i) * D : nullptr);
-        });
-    };
-    auto load_landmarks = [&](int bh) {
-        const size_t base = (size_t)bh * kT;
-        load_tile<D>(smem_u32(sHi), [&](int i) { return Qhi + (base + (i < 0 ? 0 : i)) * D; });
-        load_tile<D>(smem_u32(sLo), [&](int i) { return Qlo + (base + (i < 0 ? 0 : i)) * D; });
-        load_tile<D>(smem_u32(sVt), [&](int i) { return Vtb + (base + (i < 0 ? 0 : i)) * D; });
-    };
-    auto ready = [&]() {  // this thread's copies landed and are visible to the MMA
+    auto head = [&](int tl) { return (t_begin + tl) / tiles_per_head; };
+    if (warp == 8) {
+        // ------------------------------------------------------- producer
+        constexpr int CPR = D / 8, RPI = 32 / CPR;
+        const int cc = lane % CPR;
+        int cur = -1, gen = 0;
+        for (int tl = 0; tl < nloc; ++tl) {
+            const int bh = head(tl);
+            const bool reload = bh != cur;
+            // the query tile first: the MMA warp needs it to issue the previous
+            // tile's deferred P Vt, which the landmark reload below waits for
+            const int st = tl % NSQ;
+            int okw = 1;
+            if (lane == 0) okw = ws_wait(&q_empty[st], ((tl / NSQ) & 1) ^ 1, status, abort_v);
+            if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+            if (lane == 0) {
+                qgen[st] = gen + (reload ? 1 : 0);
+                mbar_expect_tx(&q_full[st], TILE);  // also publishes qgen
+                const int y = bh * N + ((t_begin + tl) % tiles_per_head) * kT;  // rows past the head: masked
+#pragma unroll
+                for (int cb = 0; cb < D / 64; ++cb)
+                    tma_load_2d(smem_u32(sQ + st * TILE) + cb * kT * 128, &tmQ, cb * 64, y, &q_full[st]);
+            }
+            __syncwarp();
+            if (reload) {
+                // every MMA on the previous head's landmarks must be done: the MMA
+                // warp commits lm_free once per head it leaves (gen - 1 so far)
+                if (gen > 0) {
+                    okw = 1;
+                    if (lane == 0) okw = ws_wait(&lm_free, (gen - 1) & 1, status, abort_v);
+                    if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+                }
+                const size_t y0 = (size_t)bh * kT;
+                for (int r0 = 0; r0 < kT; r0 += RPI) {
+                    const int r = r0 + lane / CPR;
+                    const size_t off = (y0 + r) * D + cc * 8;
+                    cp_async16(smem_u32(sHi) + sw_off(r, cc, kT), Qhi + off, true);
+                    cp_async16(smem_u32(sLo) + sw_off(r, cc, kT), Qlo + off, true);
+                    cp_async16(smem_u32(sVt) + sw_off(r, cc, kT), Vtb + off, true);
+                }
+                cp_async_arrive(&lm_full);
+                ++gen;
+                cur = bh;
+            }
+        }
         cp_async_wait_all();
-        fence_proxy_async();
-        __syncthreads();
-    };
-    auto issue_r = [&](int b) {
-        if (r == 0) {
+    } else if (warp == 9) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = true, pending = false;
+            int ptl = 0, cur_gen = 0;
+            auto flush = [&]() -> bool {
+                const int ob = ptl & 1;
+                if (!ws_wait(&p_full[ptl & 1], (ptl >> 1) & 1, status, abort_v)) return false;
+                if (!ws_wait(&o_free[ob], ((ptl >> 1) & 1) ^ 1, status, abort_v)) return false;
+                fence_after_sync();
+                issue_pv_ts<D>(tmem + kO0 + ob * D, tmem + kR0 + (ptl & 1) * 128, smem_u32(sVt), false);
+                mma_commit(&o_full[ob]);
+                pending = false;
+                return true;
+            };
+            for (int tl = 0; tl < nloc; ++tl) {
+                const int st = tl % NSQ, rb = tl & 1;
+                if (!(ok = ws_wait(&q_full[st], (tl / NSQ) & 1, status, abort_v))) break;
+                const int gen = qgen[st];
+                if (gen != cur_gen) {
+                    // new landmarks: the previous tile's P Vt first, then release the old
+                    // landmarks (the commit arrives when every MMA so far is done)
+                    if (pending && !(ok = flush())) break;
+                    if (cur_gen > 0) mma_commit(&lm_free);
+                    if (!(ok = ws_wait(&lm_full, (gen - 1) & 1, status, abort_v))) break;
+                    fence_proxy_async();  // landmarks came through cp.async (generic proxy)
+                    cur_gen = gen;
+                }
+                fence_after_sync();
+                issue_qk<D>(tmem + kR0 + rb * 128, smem_u32(sQ + st * TILE), smem_u32(sHi), false);
+                issue_qk<D>(tmem + kR0 + rb * 128, smem_u32(sQ + st * TILE), smem_u32(sLo), true);
+                mma_commit(&r_full[rb]);
+                mma_commit(&q_empty[st]);
+                if (pending && !(ok = flush())) break;
+                pending = true;
+                ptl = tl;
+            }
+            if (ok && pending) flush();
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------- softmax + epilogue
+        const int wg = warp >> 2, r = threadIdx.x & 127;
+        for (int tl = 0; tl < nloc; ++tl) {
+            const int rb = tl & 1, ob = tl & 1;
+            const int bh = head(tl), q = ((t_begin + tl) % tiles_per_head) * kT + r;
+            const bool q_ok = q < N;
+            if (!__all_sync(0xffffffffu, ws_wait(&r_full[rb], (tl >> 1) & 1, status, abort_v))) break;
             fence_after_sync();
-            issue_qk<D>(tmem + b * kT, smem_u32(sQb[b]), smem_u32(sHi), false);
-            issue_qk<D>(tmem + b * kT, smem_u32(sQb[b]), smem_u32(sLo), true);
-            mma_commit(&bar_r);
-        }
-    };
-
-    auto head = [&](int t) { return t / tiles_per_head; };
-    int t = t_begin, b = 0;
-    load_landmarks(head(t));
-    load_q(t, 0);
-    ready();
-    issue_r(0);
-    bool r_pending = true;  // R of tile t issued, not yet waited for
-    if (t + 1 < t_end && head(t + 1) == head(t)) load_q(t + 1, 1);
-    for (; t < t_end; ++t, b ^= 1) {
-        const int tn = t + 1;
-        const bool has_next = tn < t_end;
-        const bool new_head = has_next && head(tn) != head(t);
-        if (r_pending && !sync_on_mma(&bar_r, phase_r, status)) break;  // R(t) complete
-        r_pending = false;
-        if (has_next && !new_head) {  // Q(t+1) was prefetched; R(t+1) runs during this epilogue
-            ready();
-            issue_r(b ^ 1);
-            r_pending = true;
-        }
-        // routes and shared-slot probabilities from this thread's row of R(t)
-        const int bh = t / tiles_per_head, q = (t % tiles_per_head) * kT + r;
-        const bool q_ok = q < N;
-        const uint32_t tR = lane_base(tmem) + b * kT;
-        float v[kT];
-        tmem_ld32(tR, v);
-        tmem_ld32(tR + 32, v + 32);
-        tmem_ld32(tR + 64, v + 64);
-        tmem_ld32(tR + 96, v + 96);
-        tmem_wait_ld();
-        uint32_t bu[SMAX];
-        int bi[SMAX];
-#pragma unroll
-        for (int u = 0; u < SMAX; ++u) { bu[u] = 0u; bi[u] = -1; }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < kT; ++j) {
-            if (j < m) top_insert<SMAX>(bu, bi, order_key(v[j]), j);
-            mx = fmaxf(mx, j < m ? v[j] * sl : -INFINITY);
-        }
-        float lsum = 0.0f;
-        uint32_t pk[64];
-#pragma unroll
-        for (int j = 0; j < kT; j += 2) {
-            const float e0 = ex2(fmaf(v[j], sl, -mx)), e1 = ex2(fmaf(v[j + 1], sl, -mx));
-            const float p0 = j < m ? e0 : 0.0f, p1 = j + 1 < m ? e1 : 0.0f;
-            lsum += p0 + p1;
-            pk[j >> 1] = pack_bf16(p0, p1);
-        }
-        tmem_store_p(tR, pk);
-        if (q_ok) {
-            int32_t* Erow = E + ((size_t)bh * N + q) * s;
-#pragma unroll
-            for (int u = 0; u < SMAX; ++u)
-                if (u < s) Erow[u] = bi[u];
-            cnt[(size_t)bh * N + q] = 0;
-        }
-        fence_before_sync();
-        __syncthreads();
-        if (r == 0) {
-            fence_after_sync();
-            issue_pv_ts<D>(tmem + kO, tmem + b * kT, smem_u32(sVt), false);
-            mma_commit(&bar_o);
-        }
-        if (!sync_on_mma(&bar_o, phase_o, status)) break;
-        {
-            float o[D];
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(lane_base(tmem) + kO + c0, o + c0);
+            const uint32_t tR = lane_base(tmem) + kR0 + rb * 128;
+            const int nval = min(64, m - 64 * wg);  // landmarks of this half
+            float v[64];
+            tmem_ld32(tR + 64 * wg, v);
+            tmem_ld32(tR + 64 * wg + 32, v + 32);
             tmem_wait_ld();
-            if (q_ok) {
-                const float inv = 1.0f / lsum;
-                uint4* dst = reinterpret_cast<uint4*>(sh_part + ((size_t)bh * N + q) * D);
+            uint32_t bu[SMAX];
+            int bi[SMAX];
 #pragma unroll
-                for (int u = 0; u < D / 8; ++u)
+            for (int u = 0; u < SMAX; ++u) { bu[u] = 0u; bi[u] = -1; }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                if (j < nval) top_insert<SMAX>(bu, bi, order_key(v[j]), 64 * wg + j);
+                mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
+            }
+            xmax[wg][r] = mx;
+#pragma unroll
+            for (int u = 0; u < SMAX; ++u) {
+                xkey[wg][r][u] = bu[u];
+                xidx[wg][r][u] = bi[u];
+            }
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xbar);
+            if (!__all_sync(0xffffffffu, ws_wait(&xbar, tl & 1, status, abort_v))) break;
+            fence_after_sync();
+            mx = fmaxf(mx, xmax[wg ^ 1][r]);
+            float lsum = 0.0f;
+            uint32_t pkd[32];
+#pragma unroll
+            for (int j = 0; j < 64; j += 2) {
+                const float e0 = ex2(fmaf(v[j], sl, -mx)), e1 = ex2(fmaf(v[j + 1], sl, -mx));
+                const float p0 = j < nval ? e0 : 0.0f, p1 = j + 1 < nval ? e1 : 0.0f;
+                lsum += p0 + p1;
+                pkd[j >> 1] = pack_bf16(p0, p1);
+            }
+            tmem_st32(tR + 32 * wg, reinterpret_cast<const float*>(pkd));
+            tmem_wait_st();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[rb]);
+            // routes: the first half's list, then the second half's entries (higher indices)
+            if (wg == 0 && q_ok) {
+                uint32_t fu[SMAX];
+                int fi[SMAX];
+#pragma unroll
+                for (int u = 0; u < SMAX; ++u) { fu[u] = xkey[0][r][u]; fi[u] = xidx[0][r][u]; }
+#pragma unroll
+                for (int u = 0; u < SMAX; ++u)
+                    if (xidx[1][r][u] >= 0) top_insert<SMAX>(fu, fi, xkey[1][r][u], xidx[1][r][u]);
+                int32_t* Erow = E + ((size_t)bh * N + q) * s;
+#pragma unroll
+                for (int u = 0; u < SMAX; ++u)
+                    if (u < s) Erow[u] = fi[u];
+                cnt[(size_t)bh * N + q] = 0;
+            }
+            // shared-slot partial: normalized P Vt, this half's output columns
+            if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (tl >> 1) & 1, status, abort_v))) break;
+            fence_after_sync();
+            float o[DH];
+#pragma unroll
+            for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(lane_base(tmem) + kO0 + ob * D + wg * DH + c0, o + c0);
+            tmem_wait_ld();
+            xl[wg][r] = lsum;
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&o_free[ob]);
+                mbar_arrive(&ebar);
+            }
+            if (!__all_sync(0xffffffffu, ws_wait(&ebar, tl & 1, status, abort_v))) break;
+            if (q_ok) {
+                const float lt = lsum + xl[wg ^ 1][r];
+                const float inv = 1.0f / lt;
+                uint4* dst = reinterpret_cast<uint4*>(sh_part + ((size_t)bh * N + q) * D + wg * DH);
+#pragma unroll
+                for (int u = 0; u < DH / 8; ++u)
                     dst[u] = make_uint4(pack_bf16(o[8 * u] * inv, o[8 * u + 1] * inv),
                                         pack_bf16(o[8 * u + 2] * inv, o[8 * u + 3] * inv),
                                         pack_bf16(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
                                         pack_bf16(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
-                sh_lse[(size_t)bh * N + q] = mx + __log2f(lsum);
+                if (wg == 0) sh_lse[(size_t)bh * N + q] = mx + __log2f(lt);
             }
         }
-        fence_before_sync();
-        __syncthreads();
-        if (has_next && new_head) {  // P Vt is done with this head's landmarks
-            load_landmarks(head(tn));
-            load_q(tn, b ^ 1);
-            ready();
-            issue_r(b ^ 1);
-            r_pending = true;
-        }
-        // Q(t) is consumed (R(t) done): prefetch Q(t+2) into its buffer
-        if (t + 2 < t_end && head(t + 2) == head(tn)) load_q(t + 2, b);
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (r < 32) tmem_dealloc(tmem, 512);
+    if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
 // Variant for m_pad > 256: one CTA per 128-query tile, landmarks streamed in
@@ -1828,14 +1920,17 @@ static cudaError_t launch_route_s(const Dims& D, const TcPlan& P, const TcWork& 
     cudaError_t e;
     const int tile = kT * DD * 2;
     if (P.resident) {  // routes + the shared-slot partial in one pass
-        const int smem = 5 * tile + 1024;
-        if ((e = set_smem(k_route_shared_tc<DD, SMAX>, smem))) return e;
+        alignas(64) CUtensorMap mq;
+        if ((e = tile_map(&mq, q, (long long)D.BH * D.N, DD))) return e;
+        constexpr int NSQ = 3;
+        const int smem = (3 + NSQ) * tile + 1024;
+        if ((e = set_smem(k_route_ws<DD, SMAX, NSQ>, smem))) return e;
         const int tph = (D.N + kT - 1) / kT;
         const int total = tph * D.BH;
         const int grid = std::min(total, num_sms());
-        k_route_shared_tc<DD, SMAX><<<grid, 128, smem, st>>>(q, W.Qhi, W.Qlo, W.Vtb, D.N, D.m, D.s, tph, total,
-                                                             D.scale * 1.4426950408889634f, E, W.cnt, W.sh_part,
-                                                             W.sh_lse, status);
+        k_route_ws<DD, SMAX, NSQ><<<grid, 320, smem, st>>>(mq, W.Qhi, W.Qlo, W.Vtb, D.N, D.m, D.s, tph, total,
+                                                           D.scale * 1.4426950408889634f, E, W.cnt, W.sh_part,
+                                                           W.sh_lse, status);
     } else if (P.m_pad <= 256) {
         const int smem = 2 * P.m_pad * DD * 2 + 2 * tile + 1024;
         if ((e = set_smem(k_route_tc<DD, SMAX>, smem))) return e;
