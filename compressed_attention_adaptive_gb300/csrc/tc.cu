@@ -28,10 +28,17 @@ using namespace tc;
 constexpr int kTraceCap = 16384;
 __device__ unsigned long long g_mita_trace[4 * kTraceCap];
 __device__ int g_mita_trace_n[4];
+__shared__ int s_mita_trace_n[4];  // one recording thread per role: plain increments
+__device__ __forceinline__ void trace_init() {
+    if (threadIdx.x < 4) s_mita_trace_n[threadIdx.x] = 0;
+}
+__device__ __forceinline__ void trace_fini() {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 4) g_mita_trace_n[threadIdx.x] = s_mita_trace_n[threadIdx.x];
+}
 __device__ __forceinline__ void trace_ev(int role, int tag) {
     if (blockIdx.x != 0 || blockIdx.y != 0) return;
-    const int i = atomicAdd(&g_mita_trace_n[role], 1);
-    if (i < kTraceCap) g_mita_trace[role * kTraceCap + i] = ((unsigned long long)clock64() << 8) | (unsigned)tag;
+    const int i = s_mita_trace_n[role]++;
+    if (i >= 0 && i < kTraceCap) g_mita_trace[role * kTraceCap + i] = ((unsigned long long)clock64() << 8) | (unsigned)tag;
 }
 #endif
 
@@ -1203,6 +1210,7 @@ __global__ void __launch_bounds__(192, 1)
         abort_flag = 0;
         fence_mbar_init();
     }
+    MITA_TRACE_INIT();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -1512,6 +1520,7 @@ __global__ void __launch_bounds__(192, 1)
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
+    MITA_TRACE_FINI();
     if (warp == 5) tmem_dealloc(tmem, 512);
 }
 
@@ -1520,11 +1529,30 @@ __global__ void __launch_bounds__(192, 1)
 // memory (k <= 256): each CTA walks a contiguous range of work tiles; the
 // tiles of one expert are adjacent, so K_(e), V_(e) are gathered once per
 // expert and reused by all its tiles. The shared slots come in as a separate
-// partial (routing kernel). Roles as in k_expert_ws; the probabilities are
-// written over the scores in TMEM and O += P V reads them from there.
+// partial (routing kernel). The probabilities are written over the scores in
+// TMEM and O += P V reads them from there.
+//
+// Chunk stream: chunk g is key chunk c = g % nex of tile g / nex. The MMA
+// warp keeps S of chunks g and g + 1 in flight while the softmax works on g
+// (S of g + 2 goes right after O += P V of g, into the buffer P of g held),
+// except across a change of resident keys, where the old keys' last O += P V
+// goes first. The softmax warps defer a tile's epilogue until they have done
+// the next tile's first chunk, so the last O += P V of a tile is never waited
+// for. Each warp stages 16 rows at a time in shared memory, so that a store
+// instruction writes whole 128-byte halves of four partial rows.
 struct ResTile {
-    int bh, e, rows, gen;  // gen: loads of the resident keys so far (this tile uses load gen - 1)
+    int bh, e, start, rows, gen;  // gen: loads of the resident keys so far (this tile uses load gen - 1)
 };
+
+// One softmax warp's epilogue staging area: 16 rows of PPR 16-byte pieces
+// (a warpgroup's half of a partial row, PPR = 8 at d = 128, 4 at d = 64);
+// piece u of row r sits at u ^ ((r / (8 / PPR)) % PPR), which keeps both the
+// row-wise writes and the piece-wise reads free of bank conflicts.
+constexpr int kStageWarp = 16 * 128;
+template <int PPR>
+__device__ __forceinline__ uint32_t stage_off(int r, int u) {
+    return (r * PPR + (u ^ ((r / (8 / PPR)) & (PPR - 1)))) << 4;
+}
 
 template <int D>
 __global__ void __launch_bounds__(320, 1)
@@ -1539,11 +1567,12 @@ __global__ void __launch_bounds__(320, 1)
     uint8_t* sQ = sm;             // 2 query tiles
     uint8_t* sK = sm + 2 * TILE;  // resident key chunks (up to 2)
     uint8_t* sV = sm + 4 * TILE;  // resident value chunks
+    uint8_t* sStage = sm + 6 * TILE;  // 8 x kStageWarp epilogue staging
 
-    __shared__ uint64_t q_full[2], q_empty[2], kv_full[2], kv_free[2], s_full[2], p_full[2], o_full[2], o_free[2];
+    __shared__ uint64_t q_full[2], q_empty[2], kv_full[2], kv_rel[2], s_full[2], p_full[2], o_full[2], o_free[2];
     __shared__ uint64_t pv_done;
     __shared__ ResTile tinfo[2];
-    __shared__ int rowq[2][kT];
+    __shared__ int rowq[2][kT];  // q << 3 | slot of each tile row, -1 past the tile's rows
     __shared__ int keyrow[kT];
     __shared__ float xmax[2][2][kT], xl[2][2][kT];  // [parity][half][row] exchange of the two softmax halves
     __shared__ uint64_t xbar[2], ebar[2];          // exchange barriers (per chunk / per tile), one arrival per warp
@@ -1564,7 +1593,7 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1 + 8);
             mbar_init(&kv_full[i], 32);
-            mbar_init(&kv_free[i], 1);
+            mbar_init(&kv_rel[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 8);
             mbar_init(&o_full[i], 1);
@@ -1578,6 +1607,7 @@ __global__ void __launch_bounds__(320, 1)
         abort_flag = 0;
         fence_mbar_init();
     }
+    MITA_TRACE_INIT();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -1587,7 +1617,6 @@ __global__ void __launch_bounds__(320, 1)
     if (warp == 8) {
         // ------------------------------------------------------- producer
         int cur_bh = -1, cur_e = -1, gen = 0;
-        int armed_q[2] = {0, 0}, armed_kv[2] = {0, 0};
         const int cc = lane % CPR;
         for (int tl = 0; tl < nloc; ++tl) {
             const int qs = tl & 1;
@@ -1599,11 +1628,10 @@ __global__ void __launch_bounds__(320, 1)
             const int bh = td.x, e = td.y, start = td.z, rows = td.w & 255;
             const bool reload = bh != cur_bh || e != cur_e;
             for (int r = lane; r < kT; r += 32) rowq[qs][r] = r < rows ? perm[(size_t)bh * N * s + start + r] : -1;
-            if (lane == 0) tinfo[qs] = ResTile{bh, e, rows, gen + (reload ? 1 : 0)};
+            if (lane == 0) tinfo[qs] = ResTile{bh, e, start, rows, gen + (reload ? 1 : 0)};
             __syncwarp();
             if (lane == 0) {  // the tile's queries are consecutive rows of Qp: one bulk copy per 64 columns
                 mbar_expect_tx(&q_full[qs], TILE);  // also publishes tinfo / rowq
-                ++armed_q[qs];
                 const int y = bh * N * s + start;
 #pragma unroll
                 for (int cb = 0; cb < D / 64; ++cb)
@@ -1616,10 +1644,11 @@ __global__ void __launch_bounds__(320, 1)
                 const int32_t* Ie = I + ((size_t)bh * m + e) * k;
                 bool okc = true;
                 for (int c = 0; c < nex; ++c) {
-                    // the previous tile's O += P V on this chunk must be done (tiles before it are)
-                    if (tl > 0) {
+                    // every MMA on the previous keys of this chunk is done: the MMA
+                    // warp commits kv_rel[c] once per change of keys (gen - 1 so far)
+                    if (gen > 0) {
                         int okw = 1;
-                        if (lane == 0) okw = ws_wait(&kv_free[c], (tl - 1) & 1, status, abort_v);
+                        if (lane == 0) okw = ws_wait(&kv_rel[c], (gen - 1) & 1, status, abort_v);
                         if (!__shfl_sync(0xffffffffu, okw, 0)) { okc = false; break; }
                     }
                     for (int r = lane; r < kT; r += 32) {
@@ -1640,7 +1669,6 @@ __global__ void __launch_bounds__(320, 1)
                         cp_async16(dk + sw_off(r, cc, kT), Kb + off, true);
                         cp_async16(dv + sw_off(r, cc, kT), Vb + off, true);
                     }
-                    ++armed_kv[c];
                     cp_async_arrive(&kv_full[c]);
                     if (lane == 0) MITA_TRACE_EV(0, 4);
                     __syncwarp();
@@ -1655,74 +1683,131 @@ __global__ void __launch_bounds__(320, 1)
     } else if (warp == 9) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int g = 0, cur_gen = 0;
-            bool pending = false, ok = true;
-            int pg = 0, pc = 0, pob = 0, ptl = 0;
-            bool pfirst = false, plast = false;
-            auto flush_pv = [&]() -> bool {
-                if (!ws_wait(&p_full[pg & 1], (pg >> 1) & 1, status, abort_v)) return false;
-                MITA_TRACE_EV(1, 14);
-                if (pfirst && !ws_wait(&o_free[pob], ((ptl >> 1) & 1) ^ 1, status, abort_v)) return false;
-                fence_after_sync();
-                issue_pv_ts<D>(tmem + kO0 + pob * 128, tmem + kS0 + (pg & 1) * 128, smem_u32(sV + pc * TILE), !pfirst);
-                mma_commit(&pv_done);
-                mma_commit(&kv_free[pc]);
-                if (plast) mma_commit(&o_full[pob]);
-                MITA_TRACE_EV(1, 15);
-                pending = false;
-                return true;
-            };
-            for (int tl = 0; tl < nloc && ok; ++tl) {
-                const int qs = tl & 1;
-                if (!(ok = ws_wait(&q_full[qs], (tl >> 1) & 1, status, abort_v))) break;
-                MITA_TRACE_EV(1, 10);
-                const int gen = tinfo[qs].gen;
-                // a reload waits for the previous tile's last O += P V: issue it now
-                if (pending && gen != cur_gen && !(ok = flush_pv())) break;
-                cur_gen = gen;
-                for (int c = 0; c < nex; ++c, ++g) {
-                    if (!(ok = ws_wait(&kv_full[c], (gen - 1) & 1, status, abort_v))) break;
+            const int G = nloc * nex;
+            int ns = 0;            // next chunk whose S is to be issued
+            int seen_tl = -1;      // last tile whose query tile was waited for
+            int s_gen = 0, cur_gen = 0;  // keys of chunk ns's tile / of the last S issued
+            bool rel_last = false, ok = true;
+            for (int g = 0; g < G && ok; ++g) {
+                // S of chunks up to g + 1
+                while (ns <= g + 1 && ns < G) {
+                    const int tl = ns / nex, c = ns - tl * nex, qs = tl & 1;
+                    if (tl != seen_tl) {
+                        if (!(ok = ws_wait(&q_full[qs], (tl >> 1) & 1, status, abort_v))) break;
+                        MITA_TRACE_EV(1, 10);
+                        s_gen = tinfo[qs].gen;
+                        seen_tl = tl;
+                    }
+                    if (s_gen != cur_gen) {
+                        if (cur_gen > 0 && ns - 1 >= g) {
+                            // the old keys' last O += P V (chunk ns - 1) goes first; the
+                            // other chunks of the old keys are done with now
+                            for (int c2 = 0; c2 < nex - 1; ++c2) mma_commit(&kv_rel[c2]);
+                            rel_last = true;
+                            break;
+                        }
+                        cur_gen = s_gen;
+                    }
+                    if (!(ok = ws_wait(&kv_full[c], (s_gen - 1) & 1, status, abort_v))) break;
                     MITA_TRACE_EV(1, 11);
                     fence_proxy_async();  // copied tiles (generic proxy) -> the MMA's async-proxy reads
                     fence_after_sync();
-                    const int sb = g & 1;
-                    issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sQ + qs * TILE), smem_u32(sK + c * TILE), false);
-                    mma_commit(&s_full[sb]);
-                    const bool last = c == nex - 1;
+                    issue_qk<D>(tmem + kS0 + (ns & 1) * 128, smem_u32(sQ + qs * TILE), smem_u32(sK + c * TILE), false);
+                    mma_commit(&s_full[ns & 1]);
+                    if (c == nex - 1) mma_commit(&q_empty[qs]);
                     MITA_TRACE_EV(1, 13);
-                    if (last) mma_commit(&q_empty[qs]);
-                    if (pending && !(ok = flush_pv())) break;
-                    pending = true;
-                    pg = g;
-                    pc = c;
-                    pob = tl & 1;
-                    ptl = tl;
-                    pfirst = c == 0;
-                    plast = last;
-                    // the tile's epilogue waits on its last O += P V: issue it now
-                    if (last && !(ok = flush_pv())) break;
+                    ++ns;
                 }
+                if (!ok) break;
+                // O += P V of chunk g
+                const int tl = g / nex, c = g - tl * nex, ob = tl & 1;
+                if (!(ok = ws_wait(&p_full[g & 1], (g >> 1) & 1, status, abort_v))) break;
+                MITA_TRACE_EV(1, 14);
+                if (c == 0 && !(ok = ws_wait(&o_free[ob], ((tl >> 1) & 1) ^ 1, status, abort_v))) break;
+                fence_after_sync();
+                issue_pv_ts<D>(tmem + kO0 + ob * 128, tmem + kS0 + (g & 1) * 128, smem_u32(sV + c * TILE), c > 0);
+                mma_commit(&pv_done);
+                if (c == nex - 1) mma_commit(&o_full[ob]);
+                if (rel_last) {
+                    mma_commit(&kv_rel[nex - 1]);
+                    rel_last = false;
+                }
+                MITA_TRACE_EV(1, 15);
             }
-            if (ok && pending) flush_pv();
         }
         __syncwarp();
     } else {
         // -------------------------------------------- softmax + epilogue
         // two warpgroups share each row: wg 0 takes keys 0..63 of a chunk and
         // output columns 0..D/2-1, wg 1 the other halves; the row max and the
-        // row sum are exchanged through shared memory (named barrier 1)
+        // row sum are exchanged through shared memory (bounded mbarrier waits)
         constexpr int DH = D / 2;
         const int wg = warp >> 2, r = threadIdx.x & 127;
+        const bool fast = sl > 0.0f;  // the row max of the scaled scores is the scaled max
+        uint8_t* stage = sStage + warp * kStageWarp;
+        // epilogue of tile pt: normalized bf16 partial rows (row pk >> 3, slot
+        // pk & 7 of head pti.bh) and their log2-sum-exp
+        auto epilogue = [&](int pt, const ResTile& pti, int pk, float pl, float pm) -> bool {
+            constexpr int PPR = DH / 8, RPI = 32 / PPR;  // pieces per half row, rows per store instruction
+            const int ob = pt & 1;
+            if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (pt >> 1) & 1, status, abort_v))) return false;
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 25);
+            fence_after_sync();
+            const uint32_t tO = lane_base(tmem) + kO0 + ob * 128 + wg * DH;
+            float o[DH];
+#pragma unroll
+            for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(tO + c0, o + c0);
+            tmem_wait_ld();
+            xl[pt & 1][wg][r] = pl;
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ebar[pt & 1]);
+            if (!__all_sync(0xffffffffu, ws_wait(&ebar[pt & 1], (pt >> 1) & 1, status, abort_v))) return false;
+            if (lane == 0) mbar_arrive(&o_free[ob]);
+            const float lt = pl + xl[pt & 1][wg ^ 1][r];
+            const float inv = pk >= 0 ? 1.0f / lt : 0.0f;
+            const size_t pr = pk >= 0 ? ((size_t)pti.bh * N + (pk >> 3)) * s + (pk & 7) : 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // lanes 16h .. 16h + 15 stage their rows
+                if ((lane >> 4) == h) {
+#pragma unroll
+                    for (int u = 0; u < PPR; ++u) {
+                        const float* x = o + 8 * u;
+                        *reinterpret_cast<uint4*>(stage + stage_off<PPR>(lane & 15, u)) =
+                            make_uint4(pack_bf16(x[0] * inv, x[1] * inv), pack_bf16(x[2] * inv, x[3] * inv),
+                                       pack_bf16(x[4] * inv, x[5] * inv), pack_bf16(x[6] * inv, x[7] * inv));
+                    }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 16 / RPI; ++i) {
+                    const int rl = i * RPI + lane / PPR, u = lane % PPR;
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(stage + stage_off<PPR>(rl, u));
+                    const size_t prr = __shfl_sync(0xffffffffu, pr, 16 * h + rl);
+                    const int pkr = __shfl_sync(0xffffffffu, pk, 16 * h + rl);
+                    if (pkr >= 0) *reinterpret_cast<uint4*>(part + prr * D + wg * DH + 8 * u) = w4;
+                }
+                __syncwarp();
+            }
+            if (wg == 0 && pk >= 0) lse[pr] = pm + __log2f(lt);
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 27);
+            return true;
+        };
         int g = 0;
-        for (int tl = 0; tl < nloc; ++tl) {
+        bool have_prev = false, ok = true;
+        ResTile pti{};
+        int ppk = -1;
+        float pl = 0.0f, pm = 0.0f;
+        for (int tl = 0; tl < nloc && ok; ++tl) {
             const int qs = tl & 1, ob = tl & 1;
             if (!__all_sync(0xffffffffu, ws_wait(&q_full[qs], (tl >> 1) & 1, status, abort_v))) break;
             if (threadIdx.x == 0) MITA_TRACE_EV(2, 20);
             const ResTile ti = tinfo[qs];
             const int pk = rowq[qs][r];
-            const int q = pk >= 0 ? pk >> 3 : -1, slot = pk >= 0 ? pk & 7 : 0;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_empty[qs]);  // tinfo / rowq read; the MMA releases the tile itself
+            const bool valid = pk >= 0;
             float mref = -INFINITY, l = 0.0f;  // l: this half's share of the row sum
-            bool ok = true;
             const uint32_t tO = lane_base(tmem) + kO0 + ob * 128 + wg * DH;
             for (int c = 0; c < nex; ++c, ++g) {
                 const int sb = g & 1;
@@ -1730,14 +1815,21 @@ __global__ void __launch_bounds__(320, 1)
                 if (threadIdx.x == 0) MITA_TRACE_EV(2, 21);
                 fence_after_sync();
                 const uint32_t tS = lane_base(tmem) + kS0 + sb * 128;
-                const int nval = q >= 0 ? min(kT, k - c * kT) - 64 * wg : 0;  // valid columns of this half
+                const int nval = valid ? min(kT, k - c * kT) - 64 * wg : 0;  // valid columns of this half
+                const bool full = __all_sync(0xffffffffu, nval >= 64) && fast;
                 float v[64];
                 tmem_ld32(tS + 64 * wg, v);
                 tmem_ld32(tS + 64 * wg + 32, v + 32);
                 tmem_wait_ld();
                 float mx = -INFINITY;
+                if (full) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
+                    for (int j = 0; j < 64; ++j) mx = fmaxf(mx, v[j]);
+                    mx *= sl;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
+                }
                 xmax[g & 1][wg][r] = mx;
                 fence_before_sync();
                 __syncwarp();
@@ -1753,12 +1845,21 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 float sum = 0.0f;
                 uint32_t pkd[32];
+                if (full) {
 #pragma unroll
-                for (int j = 0; j < 64; j += 2) {
-                    const float e0 = ex2(fmaf(v[j], sl, -mnew)), e1 = ex2(fmaf(v[j + 1], sl, -mnew));
-                    const float p0 = j < nval ? e0 : 0.0f, p1 = j + 1 < nval ? e1 : 0.0f;
-                    sum += p0 + p1;
-                    pkd[j >> 1] = pack_bf16(p0, p1);
+                    for (int j = 0; j < 64; j += 2) {
+                        const float p0 = ex2(fmaf(v[j], sl, -mnew)), p1 = ex2(fmaf(v[j + 1], sl, -mnew));
+                        sum += p0 + p1;
+                        pkd[j >> 1] = pack_bf16(p0, p1);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; j += 2) {
+                        const float e0 = ex2(fmaf(v[j], sl, -mnew)), e1 = ex2(fmaf(v[j + 1], sl, -mnew));
+                        const float p0 = j < nval ? e0 : 0.0f, p1 = j + 1 < nval ? e1 : 0.0f;
+                        sum += p0 + p1;
+                        pkd[j >> 1] = pack_bf16(p0, p1);
+                    }
                 }
                 // P (bf16, two keys per column) over the scores: keys 64wg.. -> columns 32wg..
                 tmem_st32(tS + 32 * wg, reinterpret_cast<const float*>(pkd));
@@ -1767,7 +1868,8 @@ __global__ void __launch_bounds__(320, 1)
                 l = l * alpha + sum;
                 mref = mnew;
                 if (__any_sync(0xffffffffu, c > 0 && alpha != 1.0f)) {
-                    // S(g) done implies PV(g-2) done: this wait can only see PV(g-1)'s phase
+                    // S(g) done implies O += P V of chunk g - 2 done: this wait can only
+                    // see chunk g - 1's phase
                     if (!__all_sync(0xffffffffu, ws_wait(&pv_done, (g - 1) & 1, status, abort_v))) { ok = false; break; }
                     fence_after_sync();
                     const float a = (c > 0) ? alpha : 1.0f;
@@ -1785,44 +1887,26 @@ __global__ void __launch_bounds__(320, 1)
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[g & 1]);
+                // the previous tile's epilogue, now that its last O += P V has had a chunk's time
+                if (c == 0 && have_prev) {
+                    if (!(ok = epilogue(tl - 1, pti, ppk, pl, pm))) break;
+                    have_prev = false;
+                }
             }
             if (threadIdx.x == 0) MITA_TRACE_EV(2, 24);
             if (!ok) break;
-            if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (tl >> 1) & 1, status, abort_v))) break;
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 25);
-            fence_after_sync();
-            float o[DH];
-#pragma unroll
-            for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(tO + c0, o + c0);
-            tmem_wait_ld();
-            xl[tl & 1][wg][r] = l;
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ebar[tl & 1]);
-            if (!__all_sync(0xffffffffu, ws_wait(&ebar[tl & 1], (tl >> 1) & 1, status, abort_v))) break;
-            if (lane == 0) {
-                mbar_arrive(&o_free[ob]);
-                mbar_arrive(&q_empty[qs]);
-            }
-            if (q >= 0) {  // this half of the normalized partial of (query, slot)
-                const float lt = l + xl[tl & 1][wg ^ 1][r];
-                const size_t pr = ((size_t)ti.bh * N + q) * s + slot;
-                const float inv = 1.0f / lt;
-                uint4* dst = reinterpret_cast<uint4*>(part + pr * D + wg * DH);
-#pragma unroll
-                for (int u = 0; u < DH / 8; ++u)
-                    dst[u] = make_uint4(pack_bf16(o[8 * u] * inv, o[8 * u + 1] * inv),
-                                        pack_bf16(o[8 * u + 2] * inv, o[8 * u + 3] * inv),
-                                        pack_bf16(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
-                                        pack_bf16(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
-                if (wg == 0) lse[pr] = mref + __log2f(lt);
-            }
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 27);
+            have_prev = true;
+            pti = ti;
+            ppk = pk;
+            pl = l;
+            pm = mref;
         }
+        if (ok && have_prev) epilogue(nloc - 1, pti, ppk, pl, pm);
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
+    MITA_TRACE_FINI();
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
@@ -2038,7 +2122,7 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
         if (P.resident) {
             alignas(64) CUtensorMap mq;
             if ((e = tile_map(&mq, W.Qp, (long long)D.BH * D.N * D.s, DD))) return e;
-            const int smem = 6 * tile + 1024;
+            const int smem = 6 * tile + 8 * kStageWarp + 1024;
             if ((e = set_smem(k_expert_res<DD>, smem))) return e;
             k_expert_res<DD><<<num_sms(), 320, smem, st>>>(mq, kk, v, I, W.perm, W.tiles, W.tile_ctr, W.part, W.lse,
                                                            D.N, D.m, D.k, D.s, sl, status);
