@@ -164,7 +164,6 @@ static Work carve(const Dims& D, void* ws, size_t* bytes) {
         if (P.resident) {
             t.sh_part = c.take<__nv_bfloat16>(BH * D.N * D.d);
             t.sh_lse = c.take<float>(BH * D.N);
-            t.Qp = c.take<__nv_bfloat16>(BH * D.N * D.s * D.d);
         }
     }
     *bytes = align_up(c.off, 1024);

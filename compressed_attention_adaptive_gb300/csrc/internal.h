@@ -84,7 +84,6 @@ struct TcWork {
     int* cnt;                        // [BH][N]
     __nv_bfloat16* sh_part;          // [BH][N][d] shared-slot partial (resident-key path)
     float* sh_lse;                   // [BH][N]
-    __nv_bfloat16* Qp;               // [BH][N*s][d] queries in bucket order (resident-key path)
 };
 
 bool tc_supported(const Dims& D);

@@ -1017,31 +1017,6 @@ __global__ void k_bucket_scatter(const int32_t* __restrict__ E, int N, int m, in
     }
 }
 
-// Same grouping, one thread per (query, slot) pair, which also copies the
-// pair's query row to its bucket position in Qp, so that each work tile's
-// queries are consecutive rows there.
-template <int D>
-__global__ void k_bucket_scatter_copy(const int32_t* __restrict__ E, const __nv_bfloat16* __restrict__ Q, int N,
-                                      int m, int s, int* __restrict__ cursors, int32_t* __restrict__ perm,
-                                      __nv_bfloat16* __restrict__ Qp) {
-    const int bh = blockIdx.y;
-    const long long pi = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (pi >= (long long)N * s) return;
-    const int q = (int)(pi / s), t = (int)(pi % s);
-    const int e = E[((size_t)bh * N + q) * s + t];
-    if (e < 0 || e >= m) return;
-    const int pos = atomicAdd(&cursors[((size_t)bh * m + e) * 2 + (t > 0)], 1);
-    const size_t row = (size_t)bh * N * s + pos;
-    perm[row] = (q << 3) | t;
-    const uint4* src = reinterpret_cast<const uint4*>(Q + ((size_t)bh * N + q) * D);
-    uint4* dst = reinterpret_cast<uint4*>(Qp + row * D);
-    uint4 v[D / 8];
-#pragma unroll
-    for (int u = 0; u < D / 8; ++u) v[u] = src[u];
-#pragma unroll
-    for (int u = 0; u < D / 8; ++u) dst[u] = v[u];
-}
-
 // Output rows from the partials: each query's s expert partials (normalized
 // bf16 rows with log2-sum-exp) and, when given, its shared-slot partial,
 // weighted by 2^(lse - max). One thread per 8 columns of a query.
@@ -1554,9 +1529,12 @@ __device__ __forceinline__ uint32_t stage_off(int r, int u) {
     return (r * PPR + (u ^ ((r / (8 / PPR)) & (PPR - 1)))) << 4;
 }
 
+// warps 0-7 softmax + epilogue, 8 .. 8 + kNPW - 1 producers, then the MMA warp
+constexpr int kNPW = 3, kResThreads = 32 * (8 + kNPW + 1);
+
 template <int D>
-__global__ void __launch_bounds__(320, 1)
-    k_expert_res(const __grid_constant__ CUtensorMap tmQp, const __nv_bfloat16* __restrict__ K,
+__global__ void __launch_bounds__(kResThreads, 1)
+    k_expert_res(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
                  const __nv_bfloat16* __restrict__ V, const int32_t* __restrict__ I, const int32_t* __restrict__ perm,
                  const int4* __restrict__ tiles, const int* __restrict__ tile_ctr, __nv_bfloat16* __restrict__ part,
                  float* __restrict__ lse, int N, int m, int k, int s, float sl, int* __restrict__ status) {
@@ -1587,12 +1565,12 @@ __global__ void __launch_bounds__(320, 1)
     const int nloc = max(0, t_end - t_begin);
     if (nloc == 0) return;
     const int nex = (k + kT - 1) / kT;  // <= 2
-    if (warp == 9) tmem_alloc(&tmem_slot, 512);
+    if (warp == 8 + kNPW) tmem_alloc(&tmem_slot, 512);
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&q_full[i], 1);
+            mbar_init(&q_full[i], 33 * kNPW);
             mbar_init(&q_empty[i], 1 + 8);
-            mbar_init(&kv_full[i], 32);
+            mbar_init(&kv_full[i], 32 * kNPW);
             mbar_init(&kv_rel[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 8);
@@ -1614,30 +1592,49 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tmem = tmem_slot;
     constexpr int CPR = D / 8, RPI = 32 / CPR;  // 16-byte chunks per row, rows per warp instruction
 
-    if (warp == 8) {
-        // ------------------------------------------------------- producer
+    if (warp >= 8 && warp < 8 + kNPW) {
+        // ------------------------------------------------------- producers
+        // all kNPW warps gather the tile's query rows and the resident keys /
+        // values (row pairs dealt round-robin); the first also writes tinfo
+        const int pw = warp - 8;
         int cur_bh = -1, cur_e = -1, gen = 0;
         const int cc = lane % CPR;
         for (int tl = 0; tl < nloc; ++tl) {
             const int qs = tl & 1;
-            int ok = 1;
-            if (lane == 0) ok = ws_wait(&q_empty[qs], ((tl >> 1) & 1) ^ 1, status, abort_v);
-            if (lane == 0) MITA_TRACE_EV(0, 1);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             const int4 td = tiles[t_begin + tl];
             const int bh = td.x, e = td.y, start = td.z, rows = td.w & 255;
             const bool reload = bh != cur_bh || e != cur_e;
-            for (int r = lane; r < kT; r += 32) rowq[qs][r] = r < rows ? perm[(size_t)bh * N * s + start + r] : -1;
-            if (lane == 0) tinfo[qs] = ResTile{bh, e, start, rows, gen + (reload ? 1 : 0)};
-            __syncwarp();
-            if (lane == 0) {  // the tile's queries are consecutive rows of Qp: one bulk copy per 64 columns
-                mbar_expect_tx(&q_full[qs], TILE);  // also publishes tinfo / rowq
-                const int y = bh * N * s + start;
-#pragma unroll
-                for (int cb = 0; cb < D / 64; ++cb)
-                    tma_load_2d(smem_u32(sQ + qs * TILE) + cb * kT * 128, &tmQp, cb * 64, y, &q_full[qs]);
+            {
+                int ok = 1;
+                if (lane == 0) ok = ws_wait(&q_empty[qs], ((tl >> 1) & 1) ^ 1, status, abort_v);
+                if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 1);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             }
-            if (lane == 0) MITA_TRACE_EV(0, 2);
+            // this warp's rows: (query, slot) from the bucket order, -1 past the tile's rows
+            for (int r = lane; r < kT; r += 32) {
+                if ((r / RPI) % kNPW != pw) continue;
+                int pk = r < rows ? perm[(size_t)bh * N * s + start + r] : -1;
+                if (pk >= 0 && (pk >> 3) >= N) {
+                    set_status(status, kStBounds);
+                    pk = -1;
+                }
+                rowq[qs][r] = pk;
+            }
+            if (pw == 0 && lane == 0) tinfo[qs] = ResTile{bh, e, start, rows, gen + (reload ? 1 : 0)};
+            __syncwarp();
+            {
+                const __nv_bfloat16* Qb = Q + (size_t)bh * N * D;
+                const uint32_t dq = smem_u32(sQ + qs * TILE);
+#pragma unroll 4
+                for (int r0 = pw * RPI; r0 < kT; r0 += kNPW * RPI) {
+                    const int r = r0 + lane / CPR, pk = rowq[qs][r];
+                    cp_async16(dq + sw_off(r, cc, kT), Qb + (size_t)(pk >= 0 ? pk >> 3 : 0) * D + cc * 8, pk >= 0);
+                }
+                cp_async_arrive(&q_full[qs]);  // counts once this thread's copies have landed
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&q_full[qs]);  // publishes this warp's rowq rows (and tinfo)
+            }
+            if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 2);
             if (reload) {
                 const __nv_bfloat16* Kb = K + (size_t)bh * N * D;
                 const __nv_bfloat16* Vb = V + (size_t)bh * N * D;
@@ -1651,7 +1648,8 @@ __global__ void __launch_bounds__(320, 1)
                         if (lane == 0) okw = ws_wait(&kv_rel[c], (gen - 1) & 1, status, abort_v);
                         if (!__shfl_sync(0xffffffffu, okw, 0)) { okc = false; break; }
                     }
-                    for (int r = lane; r < kT; r += 32) {
+                    for (int r = lane; r < kT; r += 32) {  // this warp's rows only
+                        if ((r / RPI) % kNPW != pw) continue;
                         const int t2 = c * kT + r;
                         int j = t2 < k ? Ie[t2] : 0;
                         if (j < 0 || j >= N) {
@@ -1663,14 +1661,14 @@ __global__ void __launch_bounds__(320, 1)
                     __syncwarp();
                     const uint32_t dk = smem_u32(sK + c * TILE), dv = smem_u32(sV + c * TILE);
 #pragma unroll 4
-                    for (int r0 = 0; r0 < kT; r0 += RPI) {
+                    for (int r0 = pw * RPI; r0 < kT; r0 += kNPW * RPI) {
                         const int r = r0 + lane / CPR;
                         const size_t off = (size_t)keyrow[r] * D + cc * 8;
                         cp_async16(dk + sw_off(r, cc, kT), Kb + off, true);
                         cp_async16(dv + sw_off(r, cc, kT), Vb + off, true);
                     }
                     cp_async_arrive(&kv_full[c]);
-                    if (lane == 0) MITA_TRACE_EV(0, 4);
+                    if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 4);
                     __syncwarp();
                 }
                 if (!okc) break;
@@ -1680,7 +1678,7 @@ __global__ void __launch_bounds__(320, 1)
             }
         }
         cp_async_wait_all();  // nothing of ours may still be in flight when the CTA exits
-    } else if (warp == 9) {
+    } else if (warp == 8 + kNPW) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const int G = nloc * nex;
@@ -1907,7 +1905,7 @@ __global__ void __launch_bounds__(320, 1)
     __syncthreads();
     fence_after_sync();
     MITA_TRACE_FINI();
-    if (warp == 9) tmem_dealloc(tmem, 512);
+    if (warp == 8 + kNPW) tmem_dealloc(tmem, 512);
 }
 
 // ------------------------------------------------------------------ host
@@ -2107,12 +2105,7 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
         dim3 grid((D.N + 255) / 256, D.BH);
         k_bucket_count<<<grid, 256, use_smem ? 8 * D.m : 0, st>>>(E, D.N, D.m, D.s, W.counts, use_smem, status);
         k_bucket_scan<<<D.BH, 512, 0, st>>>(W.counts, D.m, D.N * D.s, W.cursors, W.toff, W.tile_ctr, W.tiles);
-        if (P.resident) {
-            dim3 g2((unsigned)(((long long)D.N * D.s + 255) / 256), D.BH);
-            k_bucket_scatter_copy<DD><<<g2, 256, 0, st>>>(E, q, D.N, D.m, D.s, W.cursors, W.perm, W.Qp);
-        } else {
-            k_bucket_scatter<<<grid, 256, 0, st>>>(E, D.N, D.m, D.s, W.cursors, W.perm);
-        }
+        k_bucket_scatter<<<grid, 256, 0, st>>>(E, D.N, D.m, D.s, W.cursors, W.perm);
         if ((e = cudaGetLastError())) return e;
         count_launch(3);
     }
@@ -2120,12 +2113,10 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
     prof_mark(st, "expert");
     {
         if (P.resident) {
-            alignas(64) CUtensorMap mq;
-            if ((e = tile_map(&mq, W.Qp, (long long)D.BH * D.N * D.s, DD))) return e;
             const int smem = 6 * tile + 8 * kStageWarp + 1024;
             if ((e = set_smem(k_expert_res<DD>, smem))) return e;
-            k_expert_res<DD><<<num_sms(), 320, smem, st>>>(mq, kk, v, I, W.perm, W.tiles, W.tile_ctr, W.part, W.lse,
-                                                           D.N, D.m, D.k, D.s, sl, status);
+            k_expert_res<DD><<<num_sms(), kResThreads, smem, st>>>(q, kk, v, I, W.perm, W.tiles, W.tile_ctr, W.part,
+                                                                   W.lse, D.N, D.m, D.k, D.s, sl, status);
             if ((e = cudaGetLastError())) return e;
             count_launch();
             prof_mark(st, "merge");
