@@ -28,15 +28,19 @@ using namespace tc;
 constexpr int kTraceCap = 16384;
 __device__ unsigned long long g_mita_trace[4 * kTraceCap];
 __device__ int g_mita_trace_n[4];
+__device__ int g_mita_trace_sel = 1;  // id of the kernel that records
 __shared__ int s_mita_trace_n[4];  // one recording thread per role: plain increments
-__device__ __forceinline__ void trace_init() {
+__shared__ int s_mita_trace_on;
+__device__ __forceinline__ void trace_init(int id) {
     if (threadIdx.x < 4) s_mita_trace_n[threadIdx.x] = 0;
+    if (threadIdx.x == 0) s_mita_trace_on = g_mita_trace_sel == id;
 }
 __device__ __forceinline__ void trace_fini() {
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 4) g_mita_trace_n[threadIdx.x] = s_mita_trace_n[threadIdx.x];
+    if (s_mita_trace_on && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 4)
+        g_mita_trace_n[threadIdx.x] = s_mita_trace_n[threadIdx.x];
 }
 __device__ __forceinline__ void trace_ev(int role, int tag) {
-    if (blockIdx.x != 0 || blockIdx.y != 0) return;
+    if (!s_mita_trace_on || blockIdx.x != 0 || blockIdx.y != 0) return;
     const int i = s_mita_trace_n[role]++;
     if (i >= 0 && i < kTraceCap) g_mita_trace[role * kTraceCap + i] = ((unsigned long long)clock64() << 8) | (unsigned)tag;
 }
@@ -51,6 +55,17 @@ template <int D> constexpr int kp_bytes() { return kT * D * 2 > kPTile ? kT * D 
 constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);  // S[128 x 128] = A[128 x d] B[128 x d]^T
 
 __device__ __forceinline__ uint32_t lane_base(uint32_t tmem) { return tmem + ((threadIdx.x & 96u) << 16); }
+
+// One warp's epilogue staging area: 16 rows of PPR 16-byte pieces
+// (a warpgroup's half of a partial row, PPR = 8 at d = 128, 4 at d = 64);
+// piece u of row r sits at u ^ ((r / (8 / PPR)) % PPR), which keeps both the
+// row-wise writes and the piece-wise reads free of bank conflicts.
+constexpr int kStageWarp = 16 * 128;
+template <int PPR>
+__device__ __forceinline__ uint32_t stage_off(int r, int u) {
+    return (r * PPR + (u ^ ((r / (8 / PPR)) & (PPR - 1)))) << 4;
+}
+
 
 
 // Thread 0 waits on the MMA barrier; everyone then syncs. Returns false (for
@@ -156,6 +171,54 @@ __device__ __forceinline__ void top_insert(uint32_t (&bu)[SMAX], int (&bi)[SMAX]
         bi[t] = gt ? i : ti;
         u = gt ? tu : u;
         i = gt ? ti : i;
+    }
+}
+
+// Largest of 64 values (a tree: six levels of independent maxima).
+__device__ __forceinline__ float max64(const float (&v)[64]) {
+    float t[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) t[j] = fmaxf(v[2 * j], v[2 * j + 1]);
+#pragma unroll
+    for (int h = 16; h >= 1; h >>= 1)
+#pragma unroll
+        for (int j = 0; j < h; ++j) t[j] = fmaxf(t[j], t[j + h]);
+    return t[0];
+}
+
+// Lowest j with v[j] == x, 64 if there is none (a tree of minima).
+__device__ __forceinline__ int first_eq64(const float (&v)[64], float x) {
+    int c[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) c[j] = v[2 * j] == x ? 2 * j : (v[2 * j + 1] == x ? 2 * j + 1 : 64);
+#pragma unroll
+    for (int h = 16; h >= 1; h >>= 1)
+#pragma unroll
+        for (int j = 0; j < h; ++j) c[j] = min(c[j], c[j + h]);
+    return c[0];
+}
+
+// The s (<= SMAX) largest of 64 scores v (masked ones at -inf), descending,
+// ties to the lower index, as order keys and indices base + j; m is max64(v).
+// Round u takes the largest remaining score and the lowest index holding it,
+// then masks that entry; v is consumed. Unused slots: key 0, index -1.
+template <int SMAX>
+__device__ __forceinline__ void top_s64(float (&v)[64], float m, int s, int base, uint32_t (&bu)[SMAX],
+                                        int (&bi)[SMAX]) {
+#pragma unroll
+    for (int u = 0; u < SMAX; ++u) {
+        bu[u] = 0u;
+        bi[u] = -1;
+        if (u < s && m > -INFINITY) {
+            const int i = first_eq64(v, m);
+            bu[u] = order_key(m);
+            bi[u] = base + i;
+            if (u + 1 < s) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) v[j] = j == i ? -INFINITY : v[j];
+                m = max64(v);
+            }
+        }
     }
 }
 
@@ -635,7 +698,7 @@ template <int D, int SMAX, int NSQ>
 __global__ void __launch_bounds__(320, 1)
     k_route_ws(const __grid_constant__ CUtensorMap tmQ, const __nv_bfloat16* __restrict__ Qhi,
                const __nv_bfloat16* __restrict__ Qlo, const __nv_bfloat16* __restrict__ Vtb, int N, int m, int s,
-               int tiles_per_head, int total_tiles, float sl, int32_t* __restrict__ E, int* __restrict__ cnt,
+               int tiles_per_head, int total_tiles, float sl, int32_t* __restrict__ E,
                __nv_bfloat16* __restrict__ sh_part, float* __restrict__ sh_lse, int* __restrict__ status) {
     constexpr int TILE = kT * D * 2;
     constexpr int DH = D / 2;
@@ -646,12 +709,13 @@ __global__ void __launch_bounds__(320, 1)
     uint8_t* sLo = sm + TILE;
     uint8_t* sVt = sm + 2 * TILE;
     uint8_t* sQ = sm + 3 * TILE;  // NSQ stages
+    uint8_t* sStage = sQ + NSQ * TILE;  // 8 x kStageWarp epilogue staging
     __shared__ uint64_t q_full[NSQ], q_empty[NSQ], r_full[2], p_full[2], o_full[2], o_free[2];
-    __shared__ uint64_t lm_full, lm_free, xbar, ebar;  // lm_free: the MMA warp is done with a head's landmarks
+    __shared__ uint64_t lm_full, lm_free, xbar, ebar, kbar;  // lm_free: the MMA warp is done with a head's landmarks
     __shared__ int qgen[NSQ];  // landmark load each query tile uses (1-based)
-    __shared__ float xmax[2][kT], xl[2][kT];
-    __shared__ uint32_t xkey[2][kT][SMAX];
-    __shared__ int xidx[2][kT][SMAX];
+    __shared__ float xmax[2][2][kT], xl[2][kT];  // xmax[tile parity][half][row]
+    __shared__ uint32_t xkey[kT][SMAX];  // the second half's s best, handed to the first
+    __shared__ int xidx[kT][SMAX];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     volatile int* abort_v = &abort_flag;
@@ -676,9 +740,11 @@ __global__ void __launch_bounds__(320, 1)
         mbar_init(&lm_free, 1);
         mbar_init(&xbar, 8);
         mbar_init(&ebar, 8);
+        mbar_init(&kbar, 4);
         abort_flag = 0;
         fence_mbar_init();
     }
+    MITA_TRACE_INIT(2);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -697,6 +763,7 @@ __global__ void __launch_bounds__(320, 1)
             const int st = tl % NSQ;
             int okw = 1;
             if (lane == 0) okw = ws_wait(&q_empty[st], ((tl / NSQ) & 1) ^ 1, status, abort_v);
+            if (lane == 0) MITA_TRACE_EV(0, 1);
             if (!__shfl_sync(0xffffffffu, okw, 0)) break;
             if (lane == 0) {
                 qgen[st] = gen + (reload ? 1 : 0);
@@ -737,16 +804,19 @@ __global__ void __launch_bounds__(320, 1)
             auto flush = [&]() -> bool {
                 const int ob = ptl & 1;
                 if (!ws_wait(&p_full[ptl & 1], (ptl >> 1) & 1, status, abort_v)) return false;
+                MITA_TRACE_EV(1, 14);
                 if (!ws_wait(&o_free[ob], ((ptl >> 1) & 1) ^ 1, status, abort_v)) return false;
                 fence_after_sync();
                 issue_pv_ts<D>(tmem + kO0 + ob * D, tmem + kR0 + (ptl & 1) * 128, smem_u32(sVt), false);
                 mma_commit(&o_full[ob]);
+                MITA_TRACE_EV(1, 15);
                 pending = false;
                 return true;
             };
             for (int tl = 0; tl < nloc; ++tl) {
                 const int st = tl % NSQ, rb = tl & 1;
                 if (!(ok = ws_wait(&q_full[st], (tl / NSQ) & 1, status, abort_v))) break;
+                MITA_TRACE_EV(1, 10);
                 const int gen = qgen[st];
                 if (gen != cur_gen) {
                     // new landmarks: the previous tile's P Vt first, then release the old
@@ -762,6 +832,7 @@ __global__ void __launch_bounds__(320, 1)
                 issue_qk<D>(tmem + kR0 + rb * 128, smem_u32(sQ + st * TILE), smem_u32(sLo), true);
                 mma_commit(&r_full[rb]);
                 mma_commit(&q_empty[st]);
+                MITA_TRACE_EV(1, 13);
                 if (pending && !(ok = flush())) break;
                 pending = true;
                 ptl = tl;
@@ -771,12 +842,65 @@ __global__ void __launch_bounds__(320, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------- softmax + epilogue
+        // a tile's epilogue (its normalized shared-slot partial) runs after the
+        // next tile's scores, so its P Vt has had that long to finish
         const int wg = warp >> 2, r = threadIdx.x & 127;
+        uint8_t* stage = sStage + warp * kStageWarp;
+        auto epilogue = [&](int pt, float lsum, float mx) -> bool {
+            constexpr int PPR = DH / 8, RPI = 32 / PPR;  // pieces per half row, rows per store instruction
+            const int ob = pt & 1;
+            const int bh = head(pt), q0 = ((t_begin + pt) % tiles_per_head) * kT, q = q0 + r;
+            if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (pt >> 1) & 1, status, abort_v))) return false;
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 25);
+            fence_after_sync();
+            float o[DH];
+#pragma unroll
+            for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(lane_base(tmem) + kO0 + ob * D + wg * DH + c0, o + c0);
+            tmem_wait_ld();
+            xl[wg][r] = lsum;
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&o_free[ob]);
+                mbar_arrive(&ebar);
+            }
+            if (!__all_sync(0xffffffffu, ws_wait(&ebar, pt & 1, status, abort_v))) return false;
+            const float lt = lsum + xl[wg ^ 1][r];
+            const float inv = 1.0f / lt;
+            const size_t row0 = (size_t)bh * N + q0 + (r & ~31);  // this warp's first row
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // lanes 16h .. 16h + 15 stage their rows
+                if ((lane >> 4) == h) {
+#pragma unroll
+                    for (int u = 0; u < PPR; ++u) {
+                        const float* x = o + 8 * u;
+                        *reinterpret_cast<uint4*>(stage + stage_off<PPR>(lane & 15, u)) =
+                            make_uint4(pack_bf16(x[0] * inv, x[1] * inv), pack_bf16(x[2] * inv, x[3] * inv),
+                                       pack_bf16(x[4] * inv, x[5] * inv), pack_bf16(x[6] * inv, x[7] * inv));
+                    }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 16 / RPI; ++i) {
+                    const int rl = 16 * h + i * RPI + lane / PPR, u = lane % PPR;
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(stage + stage_off<PPR>(rl - 16 * h, u));
+                    if (q0 + (r & ~31) + rl < N)
+                        *reinterpret_cast<uint4*>(sh_part + (row0 + rl) * D + wg * DH + 8 * u) = w4;
+                }
+                __syncwarp();
+            }
+            if (wg == 0 && q < N) sh_lse[(size_t)bh * N + q] = mx + __log2f(lt);
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 27);
+            return true;
+        };
+        bool ok = true;
+        float plsum = 0.0f, pmx = 0.0f;
         for (int tl = 0; tl < nloc; ++tl) {
-            const int rb = tl & 1, ob = tl & 1;
+            const int rb = tl & 1;
             const int bh = head(tl), q = ((t_begin + tl) % tiles_per_head) * kT + r;
             const bool q_ok = q < N;
-            if (!__all_sync(0xffffffffu, ws_wait(&r_full[rb], (tl >> 1) & 1, status, abort_v))) break;
+            if (!__all_sync(0xffffffffu, ws_wait(&r_full[rb], (tl >> 1) & 1, status, abort_v))) { ok = false; break; }
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 21);
             fence_after_sync();
             const uint32_t tR = lane_base(tmem) + kR0 + rb * 128;
             const int nval = min(64, m - 64 * wg);  // landmarks of this half
@@ -784,28 +908,23 @@ __global__ void __launch_bounds__(320, 1)
             tmem_ld32(tR + 64 * wg, v);
             tmem_ld32(tR + 64 * wg + 32, v + 32);
             tmem_wait_ld();
-            uint32_t bu[SMAX];
-            int bi[SMAX];
+            // this half's landmarks only: the others at -inf
 #pragma unroll
-            for (int u = 0; u < SMAX; ++u) { bu[u] = 0u; bi[u] = -1; }
-            float mx = -INFINITY;
+            for (int j = 0; j < 64; ++j) v[j] = j < nval ? v[j] : -INFINITY;
+            const float hmax = max64(v);  // largest raw score of this half
+            float mx = hmax * sl;
+            if (!(sl > 0.0f)) {  // a negative scale turns the smallest score into the largest logit
+                mx = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                if (j < nval) top_insert<SMAX>(bu, bi, order_key(v[j]), 64 * wg + j);
-                mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
+                for (int j = 0; j < 64; ++j) mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
             }
-            xmax[wg][r] = mx;
-#pragma unroll
-            for (int u = 0; u < SMAX; ++u) {
-                xkey[wg][r][u] = bu[u];
-                xidx[wg][r][u] = bi[u];
-            }
+            xmax[tl & 1][wg][r] = mx;
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&xbar);
-            if (!__all_sync(0xffffffffu, ws_wait(&xbar, tl & 1, status, abort_v))) break;
+            if (!__all_sync(0xffffffffu, ws_wait(&xbar, tl & 1, status, abort_v))) { ok = false; break; }
             fence_after_sync();
-            mx = fmaxf(mx, xmax[wg ^ 1][r]);
+            mx = fmaxf(mx, xmax[tl & 1][wg ^ 1][r]);
             float lsum = 0.0f;
             uint32_t pkd[32];
 #pragma unroll
@@ -820,53 +939,43 @@ __global__ void __launch_bounds__(320, 1)
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[rb]);
-            // routes: the first half's list, then the second half's entries (higher indices)
-            if (wg == 0 && q_ok) {
-                uint32_t fu[SMAX];
-                int fi[SMAX];
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 22);
+            // routes: this half's s best (v is consumed), the second half's list
+            // handed to the first, which merges it after its own (higher indices)
+            uint32_t bu[SMAX];
+            int bi[SMAX];
+            top_s64<SMAX>(v, hmax, s, 64 * wg, bu, bi);
+            if (wg == 1) {
 #pragma unroll
-                for (int u = 0; u < SMAX; ++u) { fu[u] = xkey[0][r][u]; fi[u] = xidx[0][r][u]; }
+                for (int u = 0; u < SMAX; ++u) {
+                    xkey[r][u] = bu[u];
+                    xidx[r][u] = bi[u];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&kbar);
+            } else {
+                if (!__all_sync(0xffffffffu, ws_wait(&kbar, tl & 1, status, abort_v))) { ok = false; break; }
+                if (q_ok) {
 #pragma unroll
-                for (int u = 0; u < SMAX; ++u)
-                    if (xidx[1][r][u] >= 0) top_insert<SMAX>(fu, fi, xkey[1][r][u], xidx[1][r][u]);
-                int32_t* Erow = E + ((size_t)bh * N + q) * s;
+                    for (int u = 0; u < SMAX; ++u)
+                        if (xidx[r][u] >= 0) top_insert<SMAX>(bu, bi, xkey[r][u], xidx[r][u]);
+                    int32_t* Erow = E + ((size_t)bh * N + q) * s;
 #pragma unroll
-                for (int u = 0; u < SMAX; ++u)
-                    if (u < s) Erow[u] = fi[u];
-                cnt[(size_t)bh * N + q] = 0;
+                    for (int u = 0; u < SMAX; ++u)
+                        if (u < s) Erow[u] = bi[u];
+                }
             }
-            // shared-slot partial: normalized P Vt, this half's output columns
-            if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (tl >> 1) & 1, status, abort_v))) break;
-            fence_after_sync();
-            float o[DH];
-#pragma unroll
-            for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(lane_base(tmem) + kO0 + ob * D + wg * DH + c0, o + c0);
-            tmem_wait_ld();
-            xl[wg][r] = lsum;
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&o_free[ob]);
-                mbar_arrive(&ebar);
-            }
-            if (!__all_sync(0xffffffffu, ws_wait(&ebar, tl & 1, status, abort_v))) break;
-            if (q_ok) {
-                const float lt = lsum + xl[wg ^ 1][r];
-                const float inv = 1.0f / lt;
-                uint4* dst = reinterpret_cast<uint4*>(sh_part + ((size_t)bh * N + q) * D + wg * DH);
-#pragma unroll
-                for (int u = 0; u < DH / 8; ++u)
-                    dst[u] = make_uint4(pack_bf16(o[8 * u] * inv, o[8 * u + 1] * inv),
-                                        pack_bf16(o[8 * u + 2] * inv, o[8 * u + 3] * inv),
-                                        pack_bf16(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
-                                        pack_bf16(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
-                if (wg == 0) sh_lse[(size_t)bh * N + q] = mx + __log2f(lt);
-            }
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 23);
+            if (tl > 0 && !(ok = epilogue(tl - 1, plsum, pmx))) break;
+            plsum = lsum;
+            pmx = mx;
         }
+        if (ok && nloc > 0) epilogue(nloc - 1, plsum, pmx);
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
+    MITA_TRACE_FINI();
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
@@ -1185,7 +1294,7 @@ __global__ void __launch_bounds__(192, 1)
         abort_flag = 0;
         fence_mbar_init();
     }
-    MITA_TRACE_INIT();
+    MITA_TRACE_INIT(1);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -1519,15 +1628,6 @@ struct ResTile {
     int bh, e, start, rows, gen;  // gen: loads of the resident keys so far (this tile uses load gen - 1)
 };
 
-// One softmax warp's epilogue staging area: 16 rows of PPR 16-byte pieces
-// (a warpgroup's half of a partial row, PPR = 8 at d = 128, 4 at d = 64);
-// piece u of row r sits at u ^ ((r / (8 / PPR)) % PPR), which keeps both the
-// row-wise writes and the piece-wise reads free of bank conflicts.
-constexpr int kStageWarp = 16 * 128;
-template <int PPR>
-__device__ __forceinline__ uint32_t stage_off(int r, int u) {
-    return (r * PPR + (u ^ ((r / (8 / PPR)) & (PPR - 1)))) << 4;
-}
 
 // warps 0-7 softmax + epilogue, 8 .. 8 + kNPW - 1 producers, then the MMA warp
 constexpr int kNPW = 3, kResThreads = 32 * (8 + kNPW + 1);
@@ -1585,7 +1685,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
         abort_flag = 0;
         fence_mbar_init();
     }
-    MITA_TRACE_INIT();
+    MITA_TRACE_INIT(1);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -2005,14 +2105,14 @@ static cudaError_t launch_route_s(const Dims& D, const TcPlan& P, const TcWork& 
         alignas(64) CUtensorMap mq;
         if ((e = tile_map(&mq, q, (long long)D.BH * D.N, DD))) return e;
         constexpr int NSQ = 3;
-        const int smem = (3 + NSQ) * tile + 1024;
+        const int smem = (3 + NSQ) * tile + 8 * kStageWarp + 1024;
         if ((e = set_smem(k_route_ws<DD, SMAX, NSQ>, smem))) return e;
         const int tph = (D.N + kT - 1) / kT;
         const int total = tph * D.BH;
         const int grid = std::min(total, num_sms());
         k_route_ws<DD, SMAX, NSQ><<<grid, 320, smem, st>>>(mq, W.Qhi, W.Qlo, W.Vtb, D.N, D.m, D.s, tph, total,
-                                                           D.scale * 1.4426950408889634f, E, W.cnt, W.sh_part,
-                                                           W.sh_lse, status);
+                                                           D.scale * 1.4426950408889634f, E, W.sh_part, W.sh_lse,
+                                                           status);
     } else if (P.m_pad <= 256) {
         const int smem = 2 * P.m_pad * DD * 2 + 2 * tile + 1024;
         if ((e = set_smem(k_route_tc<DD, SMAX>, smem))) return e;
@@ -2154,5 +2254,9 @@ extern "C" int mita_trace_read(unsigned long long* host, int* counts) {
     int zero[4] = {0, 0, 0, 0};
     cudaMemcpyToSymbol(mita::g_mita_trace_n, zero, sizeof zero);
     return 0;
+}
+// Trace builds only: which kernel records (1 expert attention, 2 routing).
+extern "C" int mita_trace_select(int id) {
+    return cudaMemcpyToSymbol(mita::g_mita_trace_sel, &id, sizeof id) == cudaSuccess ? 0 : -1;
 }
 #endif
