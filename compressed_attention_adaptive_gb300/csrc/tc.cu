@@ -174,6 +174,18 @@ __device__ __forceinline__ void top_insert(uint32_t (&bu)[SMAX], int (&bi)[SMAX]
     }
 }
 
+// Stores (score bits, key) at base[n] if pass, and counts it: a predicated
+// store, so that a sparse stream of passing scores costs no branches.
+__device__ __forceinline__ void emit_cand(int2* base, int& n, float score, int key, bool pass) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %3, 0;\n\t"
+        "@p st.global.v2.b32 [%0], {%1, %2};\n\t}" ::"l"(base + n),
+        "r"(__float_as_int(score)), "r"(key), "r"((uint32_t)pass)
+        : "memory");
+    n += pass ? 1 : 0;
+}
+
 // Largest of 64 values (a tree: six levels of independent maxima).
 __device__ __forceinline__ float max64(const float (&v)[64]) {
     float t[32];
@@ -363,6 +375,7 @@ __global__ void __launch_bounds__(320, 1)
         abort_flag = 0;
         fence_mbar_init();
     }
+    MITA_TRACE_INIT(3);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -384,6 +397,7 @@ __global__ void __launch_bounds__(320, 1)
             for (int c = 0; c < nc; ++c) {
                 const int st = c % NS, use = c / NS;
                 if (!ws_wait(&kv_empty[st], (use & 1) ^ 1, status, abort_v)) break;
+                MITA_TRACE_EV(0, 3);
                 mbar_expect_tx(&kv_full[st], 2 * TILE);
                 const int y = bh * N + j_begin + c * kT;  // rows past the split are masked, past the end read 0
 #pragma unroll
@@ -402,6 +416,7 @@ __global__ void __launch_bounds__(320, 1)
             fence_proxy_async();  // the landmark tiles came through cp.async (generic proxy)
             auto flush_pv = [&](int h) -> bool {
                 if (!ws_wait(&p_full[h & 1], (h >> 1) & 1, status, abort_v)) return false;
+                MITA_TRACE_EV(1, 14);
                 fence_after_sync();
                 issue_pv_ts<D>(tmem + kO, tmem + kS0 + (h & 1) * 128, smem_u32(sV + (h % NS) * TILE), h > 0);
                 mma_commit(&pv_done);
@@ -412,10 +427,12 @@ __global__ void __launch_bounds__(320, 1)
             for (int c = 0; c < nc && ok; ++c) {
                 const int st = c % NS, sb = c & 1;
                 if (!(ok = ws_wait(&kv_full[st], (c / NS) & 1, status, abort_v))) break;
+                MITA_TRACE_EV(1, 11);
                 fence_after_sync();
                 issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sHi), smem_u32(sK + st * TILE), false);
                 issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sLo), smem_u32(sK + st * TILE), true);
                 mma_commit(&s_full[sb]);
+                MITA_TRACE_EV(1, 13);
                 if (c > 0 && !(ok = flush_pv(c - 1))) break;
             }
             if (ok) flush_pv(nc - 1);
@@ -437,6 +454,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < nc; ++c) {
             const int sb = c & 1, j0 = j_begin + c * kT;
             if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (c >> 1) & 1, status, abort_v))) { ok = false; break; }
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 21);
             fence_after_sync();
             const uint32_t tS = lane_base(tmem) + kS0 + sb * 128;
             const int nval = row_ok ? min(kT, j_end - j0) - 64 * wg : 0;
@@ -445,12 +463,19 @@ __global__ void __launch_bounds__(320, 1)
             tmem_ld32(tS + 64 * wg + 32, v + 32);
             tmem_wait_ld();
             float mx = -INFINITY;
+            if (nval >= 64 && sl > 0.0f) {  // every column real: one tree maximum
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                if (j < nval && v[j] >= th) cw[ncand++] = make_int2(__float_as_int(v[j]), j0 + 64 * wg + j);
-                mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
+                for (int j = 0; j < 64; ++j) emit_cand(cw, ncand, v[j], j0 + 64 * wg + j, v[j] >= th);
+                mx = max64(v) * sl;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    emit_cand(cw, ncand, v[j], j0 + 64 * wg + j, j < nval && v[j] >= th);
+                    mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
+                }
             }
             xmax[c & 1][wg][r] = mx;
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 23);
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&xbar[c & 1]);
@@ -494,6 +519,7 @@ __global__ void __launch_bounds__(320, 1)
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[c & 1]);
+            if (threadIdx.x == 0) MITA_TRACE_EV(2, 22);
         }
         if (ok && __all_sync(0xffffffffu, ws_wait(&o_full, 0, status, abort_v))) {
             fence_after_sync();
@@ -519,6 +545,7 @@ __global__ void __launch_bounds__(320, 1)
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
+    MITA_TRACE_FINI();
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
