@@ -16,6 +16,43 @@
 
 namespace mita {
 
+// Digit search of one radix pass, by warp 0: the largest bin b such that the
+// bins b..255 hold at least `rem` keys (bin 0 if none does), the count in the
+// bins above b (*above) and in b itself (*in_b). Lane L holds bins
+// 255 - 8L .. 248 - 8L; a shuffle prefix sum over lanes finds the lane where
+// the running count from the top reaches rem, which then scans its 8 bins.
+// Returns true on the one lane that found it.
+__device__ __forceinline__ bool radix_digit(const unsigned* hist, int rem, int* b_out, int* above, int* in_b) {
+    const int lane = threadIdx.x & 31;
+    int c[8], lsum = 0;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        c[t] = (int)hist[255 - 8 * lane - t];
+        lsum += c[t];
+    }
+    int incl = lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const unsigned ball = __ballot_sync(0xffffffffu, incl >= rem);
+    const int L = ball ? __ffs(ball) - 1 : 31;
+    if (lane != L) return false;
+    int acc = incl - lsum;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        if (t == 7 || acc + c[t] >= rem) {
+            *b_out = 255 - 8 * lane - t;
+            *above = acc;
+            *in_b = c[t];
+            return true;
+        }
+        acc += c[t];
+    }
+    return true;
+}
+
 // Shared part of both selectors: finds (v, rem) over n keys produced by
 // key_of(j). All threads of the block return the same values.
 template <typename KeyOf>
@@ -33,14 +70,12 @@ __device__ __forceinline__ void radix_kth(int n, int k, KeyOf key_of, unsigned* 
             if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
-            int acc = 0, b = 255;
-            for (; b > 0; --b) {
-                if (acc + (int)hist[b] >= rem) break;
-                acc += (int)hist[b];
+        if (threadIdx.x < 32) {
+            int b, acc, in_b;
+            if (radix_digit(hist, rem, &b, &acc, &in_b)) {
+                sh_prefix = prefix | ((uint32_t)b << shift);
+                sh_rem = rem - acc;
             }
-            sh_prefix = prefix | ((uint32_t)b << shift);
-            sh_rem = rem - acc;
         }
         __syncthreads();
         prefix = sh_prefix;
@@ -146,15 +181,13 @@ __device__ __forceinline__ uint32_t radix_select(const CandSrc& cs, int rem, Key
             if (ok && (u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
         });
         __syncthreads();
-        if (threadIdx.x == 0) {
-            int acc = 0, b = 255;
-            for (; b > 0; --b) {
-                if (acc + (int)hist[b] >= rem) break;
-                acc += (int)hist[b];
+        if (threadIdx.x < 32) {
+            int b, acc, in_b;
+            if (radix_digit(hist, rem, &b, &acc, &in_b)) {
+                sh_prefix = prefix | ((uint32_t)b << shift);
+                sh_rem = rem - acc;
+                sh_eq = in_b;
             }
-            sh_prefix = prefix | ((uint32_t)b << shift);
-            sh_rem = rem - acc;
-            sh_eq = (int)hist[b];
         }
         __syncthreads();
         prefix = sh_prefix;
