@@ -178,8 +178,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--B", type=int, default=None, help="override the batch (small profiling cases)")
     ap.add_argument("--H", type=int, default=None, help="override the heads (small profiling cases)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every configuration (vision, 32k, 131k and the m/k/s sweep) against its roofline, "
+                         "one JSON line each, instead of the benchmark line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed steps
+    if args.sweep:
+        sweep(args)
+        return
 
     from compressed_attention_adaptive_gb300 import synth
     w = synth.get(args.workload)
@@ -275,6 +281,49 @@ def main():
                                           % (n_heads, w.BH, w.N), "seconds": t}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def sweep(args):
+    """Per configuration: step time (CUDA events over --steps steps after
+    --warmup), t_roof = max(F / bf16 peak, bytes / HBM peak) and their ratio."""
+    import numpy as np
+    import torch
+    import compressed_attention_adaptive_gb300 as mita
+    from compressed_attention_adaptive_gb300 import synth
+    dev = torch.device("cuda", 0)
+    pk, pk_src = peaks()
+    names = ["vision_128x128", "longctx_n32k", "n131k"] + [w.name for w in synth.sweep_workloads()]
+    for name in names:
+        w = synth.get(name)
+        Qn, Kn, Vn = synth.make_inputs(w, seed=0)
+        tt = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev) if w.dtype == "bf16" \
+            else torch.from_numpy(a).to(dev)
+        Q, K, V = tt(Qn), tt(Kn), tt(Vn)
+        O = torch.empty_like(Q)
+        p = mita.params_for(Q, w.m, w.k, w.s, w.grid, w.lm)
+        ws = mita.workspace(p, dev)
+        stream = torch.cuda.current_stream(dev)
+        for _ in range(args.warmup):
+            mita.mita_forward(p, Q, K, V, O, ws)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            mita.mita_forward(p, Q, K, V, O, ws)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        mita.mita_device_status(ws)
+        ms = e0.elapsed_time(e1) / args.steps
+        F, Bytes, _ = work_counts(w)
+        t_f, t_b = F / (pk["bf16_tflops"] * 1e12), Bytes / (pk["hbm_gbs"] * 1e9)
+        t_roof = max(t_f, t_b)
+        print(json.dumps({"workload": name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "m": w.m, "k": w.k, "s": w.s,
+                          "ms_per_step": ms, "value": w.BH * w.N / (ms * 1e-3), "unit": UNIT,
+                          "flops": F, "compulsory_bytes": Bytes, "bound": "tensor" if t_f >= t_b else "hbm",
+                          "t_roof_us": t_roof * 1e6, "frac": t_roof / (ms * 1e-3), "peaks": pk_src,
+                          "path": "tcgen05" if mita.mita_uses_tensor_cores(p) == 1 else "cuda-core"}), flush=True)
+        del Q, K, V, O, ws
+        torch.cuda.empty_cache()
 
 
 def e2e_run(mita, p, Qn, Kn, Vn, w, dev, steps, dist, world):
