@@ -584,18 +584,32 @@ __global__ void k_vt_combine(const float* __restrict__ Opart, const float2* __re
 template <int SMAX>
 __device__ __forceinline__ void route_epilogue(uint32_t tR, int m, int s, int q, bool q_ok, int32_t* __restrict__ Erow,
                                                int* __restrict__ cnt_q) {
+    // the SMAX best landmarks so far (s <= SMAX of them are written), descending,
+    // ties to the lower index; blocks of 64 are visited in increasing index order,
+    // and a block only contributes while its largest remaining score beats the
+    // SMAX-th best (an equal score has a higher index and ranks behind)
     uint32_t bu[SMAX];
     int bi[SMAX];
 #pragma unroll
     for (int t = 0; t < SMAX; ++t) { bu[t] = 0u; bi[t] = -1; }
 #pragma unroll 1
-    for (int c0 = 0; c0 < m; c0 += 32) {
-        float v[32];
+    for (int c0 = 0; c0 < m; c0 += 64) {
+        float v[64];
         tmem_ld32(tR + c0, v);
+        tmem_ld32(tR + c0 + 32, v + 32);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (c0 + j < m) top_insert<SMAX>(bu, bi, order_key(v[j]), c0 + j);
+        for (int j = 0; j < 64; ++j) v[j] = c0 + j < m ? v[j] : -INFINITY;
+        float mx = max64(v);
+#pragma unroll 1
+        for (int u = 0; u < SMAX; ++u) {
+            if (!(mx > -INFINITY) || order_key(mx) <= bu[SMAX - 1]) break;
+            const int i = first_eq64(v, mx);
+            top_insert<SMAX>(bu, bi, order_key(mx), c0 + i);
+#pragma unroll
+            for (int j = 0; j < 64; ++j) v[j] = j == i ? -INFINITY : v[j];
+            mx = max64(v);
+        }
     }
     if (q_ok) {
 #pragma unroll
