@@ -1289,13 +1289,18 @@ struct WsMeta {  // what the deferred O += P V of a chunk needs
     bool first, last;
 };
 
+// producer warps of the expert-attention kernels (they share the gathers of
+// query rows and keys / values); streaming kernel: warps 0-3 softmax +
+// epilogue, 4 .. 4 + kNPW - 1 producers, then the MMA warp
+constexpr int kNPW = 3, kWsThreads = 32 * (4 + kNPW + 1);
+
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kWsThreads, 1)
     k_expert_ws(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
                 const __nv_bfloat16* __restrict__ V, const __nv_bfloat16* __restrict__ Qhi,
                 const __nv_bfloat16* __restrict__ Vtb, const int32_t* __restrict__ I,
                 const int32_t* __restrict__ perm, const int4* __restrict__ tiles, const int* __restrict__ tile_ctr,
-                int* __restrict__ tile_next, __nv_bfloat16* __restrict__ O, __nv_bfloat16* __restrict__ part,
+                __nv_bfloat16* __restrict__ O, __nv_bfloat16* __restrict__ part,
                 float* __restrict__ lse, int* __restrict__ cnt, int N, int m, int m_pad, int k, int s, int shared_on,
                 float sl, int* __restrict__ status) {
     constexpr int TILE = kT * D * 2;
@@ -1317,12 +1322,16 @@ __global__ void __launch_bounds__(192, 1)
     volatile int* abort_v = &abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == 5) tmem_alloc(&tmem_slot, 512);
+    const int ntiles = *(volatile const int*)tile_ctr;
+    const int per = (ntiles + gridDim.x - 1) / gridDim.x;
+    const int t_begin = blockIdx.x * per, nloc = max(0, min(ntiles, t_begin + per) - t_begin);
+    if (nloc == 0) return;
+    if (warp == 4 + kNPW) tmem_alloc(&tmem_slot, 512);
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&q_full[i], 32 + 1);  // 32 copy-completion arrivals + the row-list publish
+            mbar_init(&q_full[i], 33 * kNPW);  // per producer warp: 32 copy completions + the row publish
             mbar_init(&q_empty[i], 1 + 4);
-            mbar_init(&kv_full[i], 32);
+            mbar_init(&kv_full[i], 32 * kNPW);
             mbar_init(&kv_empty[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 4);
@@ -1340,62 +1349,55 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = tmem_slot;
-    const int ntiles = *(volatile const int*)tile_ctr;
     const int nex = (k + kT - 1) / kT;
     const int nsh_full = shared_on ? (m + kT - 1) / kT : 0;
 
-    if (warp == 4) {
-        // ------------------------------------------------------- producer
-        int tseq = 0, g = 0;
-        int armed_q[2] = {0, 0}, armed_kv[2] = {0, 0};
-        for (;;) {
+    if (warp >= 4 && warp < 4 + kNPW) {
+        // ------------------------------------------------------- producers
+        // all kNPW warps gather (row pairs dealt round-robin); the first also
+        // writes the tile info
+        const int pw = warp - 4;
+        int g = 0;
+        for (int tseq = 0; tseq < nloc; ++tseq) {
             const int qs = tseq & 1;
             int ok = 1;
             if (lane == 0) ok = ws_wait(&q_empty[qs], ((tseq >> 1) & 1) ^ 1, status, abort_v);
-            if (lane == 0) MITA_TRACE_EV(0, 1);
+            if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 1);
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            int t = 0;
-            if (lane == 0) t = atomicAdd(tile_next, 1);
-            t = __shfl_sync(0xffffffffu, t, 0);
-            if (t >= ntiles) {
-                if (lane == 0) tinfo[qs].rows = -1;
-                __syncwarp();
-                mbar_arrive(&q_full[qs]);
-                if (lane == 0) mbar_arrive(&q_full[qs]);
-                break;
-            }
-            const int4 td = tiles[t];
+            const int4 td = tiles[t_begin + tseq];
             const int bh = td.x, e = td.y, start = td.z, rows = td.w & 255, shrows = td.w >> 8;
             const int nsh = shrows > 0 ? nsh_full : 0;
             const int nch = nsh + nex;
             // row indices go to shared memory; the copies then run two rows per
             // warp instruction (16 lanes x 16 bytes per 256-byte row for d = 128)
             const int rbase = bh * N;
-            for (int r = lane; r < kT; r += 32) rowq[qs][r] = r < rows ? perm[(size_t)bh * N * s + start + r] : -1;
-            if (lane == 0) tinfo[qs] = WsTile{bh, e, rows, shrows, nsh, nch};
-            __syncwarp();
             constexpr int CPR = D / 8;        // 16-byte chunks per row
             constexpr int RPI = 32 / CPR;     // rows per warp instruction
+            for (int r = lane; r < kT; r += 32)
+                if ((r / RPI) % kNPW == pw) rowq[qs][r] = r < rows ? perm[(size_t)bh * N * s + start + r] : -1;
+            if (pw == 0 && lane == 0) tinfo[qs] = WsTile{bh, e, rows, shrows, nsh, nch};
+            __syncwarp();
             {
                 const uint32_t dst = smem_u32(sQ + qs * TILE);
                 const int cc = lane % CPR;
 #pragma unroll 4
-                for (int r0 = 0; r0 < kT; r0 += RPI) {
+                for (int r0 = pw * RPI; r0 < kT; r0 += kNPW * RPI) {
                     const int r = r0 + lane / CPR;
                     const int pk = rowq[qs][r];
                     const __nv_bfloat16* src = Q + ((size_t)rbase + (pk >= 0 ? (pk >> 3) : 0)) * D + cc * 8;
                     cp_async16(dst + sw_off(r, cc, kT), src, true);
                 }
-                ++armed_q[qs];
                 cp_async_arrive(&q_full[qs]);
-                if (lane == 0) mbar_arrive(&q_full[qs]);  // publishes tinfo / rowq
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&q_full[qs]);  // publishes this warp's rowq rows (and tinfo)
             }
-            if (lane == 0) MITA_TRACE_EV(0, 2);
+            if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 2);
             // key rows of chunk c into keyrow[buf]: landmark rows for the shared
             // chunks, I_e entries for the expert's chunks
             auto load_keys = [&](int c, int buf) {
                 const bool shc = c < nsh;
                 for (int r = lane; r < kT; r += 32) {
+                    if ((r / RPI) % kNPW != pw) continue;  // this warp's rows only
                     int row;
                     if (shc) {
                         row = c * kT + r;  // < m_pad since c < ceil(m / 128)
@@ -1417,7 +1419,7 @@ __global__ void __launch_bounds__(192, 1)
                 const int st = g & 1;
                 int okw = 1;
                 if (lane == 0) okw = ws_wait(&kv_empty[st], ((g >> 1) & 1) ^ 1, status, abort_v);
-                if (lane == 0) MITA_TRACE_EV(0, 3);
+                if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 3);
                 if (!__shfl_sync(0xffffffffu, okw, 0)) { ok2 = false; break; }
                 __syncwarp();
                 {
@@ -1428,38 +1430,24 @@ __global__ void __launch_bounds__(192, 1)
                     const int* kr = keyrow[g & 1];
                     const int cc = lane % CPR;
 #pragma unroll 4
-                    for (int r0 = 0; r0 < kT; r0 += RPI) {
+                    for (int r0 = pw * RPI; r0 < kT; r0 += kNPW * RPI) {
                         const int r = r0 + lane / CPR;
                         const size_t off = (size_t)kr[r] * D + cc * 8;
                         cp_async16(dk + sw_off(r, cc, kT), kb + off, true);
                         cp_async16(dv + sw_off(r, cc, kT), vb + off, true);
                     }
-                    ++armed_kv[st];
                     cp_async_arrive(&kv_full[st]);
                 }
-                if (lane == 0) MITA_TRACE_EV(0, 4);
+                if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 4);
                 // the next chunk's key rows load while this stage fills and the next one drains
                 if (c + 1 < nch) load_keys(c + 1, (g + 1) & 1);
-                if (lane == 0) MITA_TRACE_EV(0, 5);
+                if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 5);
                 __syncwarp();
             }
             if (!ok2) break;
-            ++tseq;
         }
-        // on abort, let the copies in flight land before the CTA exits
-        if (lane == 0 && *abort_v) {
-            for (int i = 0; i < 2; ++i) {
-                if (armed_q[i]) {
-                    const long long t0 = clock64();
-                    while (!mbar_try_wait(&q_full[i], (armed_q[i] - 1) & 1) && clock64() - t0 < (1LL << 27)) {}
-                }
-                if (armed_kv[i]) {
-                    const long long t0 = clock64();
-                    while (!mbar_try_wait(&kv_full[i], (armed_kv[i] - 1) & 1) && clock64() - t0 < (1LL << 27)) {}
-                }
-            }
-        }
-    } else if (warp == 5) {
+        cp_async_wait_all();  // nothing of ours may still be in flight when the CTA exits
+    } else if (warp == 4 + kNPW) {
         // ------------------------------------------------------ MMA issuer
         // strict order: S(g), then the deferred O += P V of chunk g-1, so the
         // tensor core computes S(g) while the softmax works on chunk g-1;
@@ -1483,7 +1471,7 @@ __global__ void __launch_bounds__(192, 1)
                 pending = false;
                 return true;
             };
-            for (;;) {
+            for (; tseq < nloc;) {
                 const int qs = tseq & 1;
                 if (!(ok = ws_wait(&q_full[qs], (tseq >> 1) & 1, status, abort_v))) break;
                 MITA_TRACE_EV(1, 10);
@@ -1517,7 +1505,7 @@ __global__ void __launch_bounds__(192, 1)
         // -------------------------------------------- softmax + epilogue
         const int r = threadIdx.x;
         int tseq = 0, g = 0;
-        for (;;) {
+        for (; tseq < nloc;) {
             const int qs = tseq & 1, ob = tseq & 1;
             if (!__all_sync(0xffffffffu, ws_wait(&q_full[qs], (tseq >> 1) & 1, status, abort_v))) break;
             if (threadIdx.x == 0) MITA_TRACE_EV(2, 20);
@@ -1646,7 +1634,7 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     fence_after_sync();
     MITA_TRACE_FINI();
-    if (warp == 5) tmem_dealloc(tmem, 512);
+    if (warp == 4 + kNPW) tmem_dealloc(tmem, 512);
 }
 
 // ------------------------------------------------------------------------
@@ -1670,8 +1658,9 @@ struct ResTile {
 };
 
 
-// warps 0-7 softmax + epilogue, 8 .. 8 + kNPW - 1 producers, then the MMA warp
-constexpr int kNPW = 3, kResThreads = 32 * (8 + kNPW + 1);
+// expert attention with resident keys: warps 0-7 softmax + epilogue,
+// 8 .. 8 + kNPW - 1 producers, then the MMA warp
+constexpr int kResThreads = 32 * (8 + kNPW + 1);
 
 template <int D>
 __global__ void __launch_bounds__(kResThreads, 1)
@@ -2267,9 +2256,10 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
         } else {
             const int smem = 4 * tile + 2 * kp_bytes<DD>() + 1024;
             if ((e = set_smem(k_expert_ws<DD>, smem))) return e;
-            k_expert_ws<DD><<<num_sms(), 192, smem, st>>>(q, kk, v, W.Qhi, W.Vtb, I, W.perm, W.tiles, W.tile_ctr,
-                                                          W.tile_ctr + 1, (__nv_bfloat16*)O, W.part, W.lse, W.cnt,
-                                                          D.N, D.m, P.m_pad, D.k, D.s, D.shared ? 1 : 0, sl, status);
+            k_expert_ws<DD><<<num_sms(), kWsThreads, smem, st>>>(q, kk, v, W.Qhi, W.Vtb, I, W.perm, W.tiles,
+                                                                 W.tile_ctr, (__nv_bfloat16*)O, W.part, W.lse, W.cnt,
+                                                                 D.N, D.m, P.m_pad, D.k, D.s, D.shared ? 1 : 0, sl,
+                                                                 status);
         }
         if ((e = cudaGetLastError())) return e;
         count_launch();
