@@ -199,6 +199,10 @@ __device__ __forceinline__ uint32_t radix_select(const CandSrc& cs, int rem, Key
     return prefix;
 }
 
+// Candidate regions (key split x column half) a row can have and still be
+// staged in shared memory.
+constexpr int kMaxRegions = 256;
+
 // Exact top-k of one landmark row from its candidates: the k-th largest score
 // key v, the lowest key indices among scores equal to v, then the chosen keys
 // marked in a bitmap and written out in ascending order. Dynamic shared
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(512) k_topk_cand(const int2* __restrict__ cand
     extern __shared__ uint32_t dyn[];
     __shared__ unsigned hist[256];
     __shared__ int tmp[33];
-    __shared__ int sh_off[65];
+    __shared__ int sh_off[kMaxRegions + 1];
     __shared__ int sh_total;
     const int bh = blockIdx.y, i = blockIdx.x;
     const size_t rrow = (size_t)bh * m_pad + i;
@@ -222,15 +226,15 @@ __global__ void __launch_bounds__(512) k_topk_cand(const int2* __restrict__ cand
     const int* cnts = ccount + rrow * splits;
     const int2* base = cand + rrow * splits * cap;
     for (int w = threadIdx.x; w < nwords; w += blockDim.x) bits[w] = 0u;
-    // region counts: read in parallel (up to 64 staged), then prefix offsets
-    __shared__ int sh_cnt[64];
-    for (int sp = threadIdx.x; sp < 64; sp += blockDim.x) sh_cnt[sp] = sp < splits ? cnts[sp] : 0;
+    // region counts: read in parallel (up to kMaxRegions staged), then prefix offsets
+    __shared__ int sh_cnt[kMaxRegions];
+    for (int sp = threadIdx.x; sp < kMaxRegions; sp += blockDim.x) sh_cnt[sp] = sp < splits ? cnts[sp] : 0;
     __syncthreads();
     if (threadIdx.x == 0) {
         int tot = 0;
         for (int sp = 0; sp < splits; ++sp) {
-            const int c = sp < 64 ? sh_cnt[sp] : cnts[sp];
-            if (sp < 64) sh_off[sp] = tot;
+            const int c = sp < kMaxRegions ? sh_cnt[sp] : cnts[sp];
+            if (sp < kMaxRegions) sh_off[sp] = tot;
             tot += c;
         }
         sh_total = tot;
@@ -244,15 +248,19 @@ __global__ void __launch_bounds__(512) k_topk_cand(const int2* __restrict__ cand
         return;
     }
     CandSrc cs{nullptr, nullptr, 0, base, cnts, splits, cap};
-    if (total <= stage_cap && splits <= 64) {  // one read of the records, the passes run in shared memory
-        for (int sp = 0; sp < splits; ++sp) {
-            const int c = sh_cnt[sp], o = sh_off[sp];
-            const int2* b = base + sp * cap;
-            for (int t = threadIdx.x; t < c; t += blockDim.x) {
-                const int2 r = b[t];
-                skey[o + t] = order_key(__int_as_float(r.x));
-                sidx[o + t] = r.y;
+    if (total <= stage_cap && splits <= kMaxRegions) {  // one read of the records, the passes run in shared memory
+        // flat over all records (independent loads): record gi sits in the last
+        // region whose offset is <= gi (empty regions share the next offset)
+        for (int gi = threadIdx.x; gi < total; gi += blockDim.x) {
+            int lo = 0, hi = splits - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (sh_off[mid] <= gi) lo = mid;
+                else hi = mid - 1;
             }
+            const int2 r = base[lo * cap + (gi - sh_off[lo])];
+            skey[gi] = order_key(__int_as_float(r.x));
+            sidx[gi] = r.y;
         }
         __syncthreads();
         cs.skey = skey;
@@ -303,9 +311,9 @@ cudaError_t launch_sample_threshold(const float* Ssamp, long long rows, int n_sa
 cudaError_t launch_topk_cand(const int2* cand, const int* ccount, int splits, long long cap, int BH, int m, int m_pad,
                              int N, int k, long long expect, int32_t* I, int* status, cudaStream_t st) {
     const int bitmap = ((N + 31) / 32) * 4;
-    // stage about three times the expected candidate count (8k at most) so
+    // stage about three times the expected candidate count (12k at most) so
     // that several rows fit on an SM; larger rows read from global memory
-    const long long want = std::min<long long>(8192, std::max<long long>(1024, 3 * expect));
+    const long long want = std::min<long long>(12288, std::max<long long>(1024, 3 * expect));
     const int stage_cap = (int)std::max<long long>(0, std::min<long long>(want, (160 * 1024 - bitmap) / 8));
     const int smem = bitmap + stage_cap * 8;
     cudaError_t e0 = cudaFuncSetAttribute(k_topk_cand, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
