@@ -1154,17 +1154,48 @@ __global__ void __launch_bounds__(512) k_bucket_scan(const int* __restrict__ cou
 }
 
 // perm[bh][pos] = q << 3 | slot, at the pair's place in its expert's bucket.
+// With use_smem, a block first ranks its pairs per (expert, class) bin in
+// shared memory, then reserves each non-empty bin's range with one global
+// atomic, instead of one contended global atomic per pair.
 __global__ void k_bucket_scatter(const int32_t* __restrict__ E, int N, int m, int s, int* __restrict__ cursors,
-                                 int32_t* __restrict__ perm) {
+                                 int32_t* __restrict__ perm, int use_smem) {
+    extern __shared__ int bins[];  // 2m local counts, then the bins' global bases
     const int bh = blockIdx.y;
     const int q = blockIdx.x * blockDim.x + threadIdx.x;
-    if (q >= N) return;
-    for (int t = 0; t < s; ++t) {
-        const int e = E[((size_t)bh * N + q) * s + t];
-        if (e < 0 || e >= m) continue;
-        const int pos = atomicAdd(&cursors[((size_t)bh * m + e) * 2 + (t > 0)], 1);
-        perm[(size_t)bh * N * s + pos] = (q << 3) | t;
+    int* cur = cursors + (size_t)bh * m * 2;
+    if (!use_smem) {
+        if (q >= N) return;
+        for (int t = 0; t < s; ++t) {
+            const int e = E[((size_t)bh * N + q) * s + t];
+            if (e < 0 || e >= m) continue;
+            const int pos = atomicAdd(&cur[e * 2 + (t > 0)], 1);
+            perm[(size_t)bh * N * s + pos] = (q << 3) | t;
+        }
+        return;
     }
+    for (int i = threadIdx.x; i < 2 * m; i += blockDim.x) bins[i] = 0;
+    __syncthreads();
+    int bin[kMaxS], rank[kMaxS];
+#pragma unroll
+    for (int t = 0; t < kMaxS; ++t) {
+        bin[t] = -1;
+        if (t < s && q < N) {
+            const int e = E[((size_t)bh * N + q) * s + t];
+            if (e >= 0 && e < m) {
+                bin[t] = e * 2 + (t > 0);
+                rank[t] = atomicAdd(&bins[bin[t]], 1);
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 2 * m; i += blockDim.x) {
+        const int c = bins[i];
+        bins[i] = c ? atomicAdd(&cur[i], c) : 0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < kMaxS; ++t)
+        if (bin[t] >= 0) perm[(size_t)bh * N * s + bins[bin[t]] + rank[t]] = (q << 3) | t;
 }
 
 // Output rows from the partials: each query's s expert partials (normalized
@@ -2235,7 +2266,7 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
         dim3 grid((D.N + 255) / 256, D.BH);
         k_bucket_count<<<grid, 256, use_smem ? 8 * D.m : 0, st>>>(E, D.N, D.m, D.s, W.counts, use_smem, status);
         k_bucket_scan<<<D.BH, 512, 0, st>>>(W.counts, D.m, D.N * D.s, W.cursors, W.toff, W.tile_ctr, W.tiles);
-        k_bucket_scatter<<<grid, 256, 0, st>>>(E, D.N, D.m, D.s, W.cursors, W.perm);
+        k_bucket_scatter<<<grid, 256, use_smem ? 8 * D.m : 0, st>>>(E, D.N, D.m, D.s, W.cursors, W.perm, use_smem);
         if ((e = cudaGetLastError())) return e;
         count_launch(3);
     }
