@@ -1906,7 +1906,9 @@ __global__ void __launch_bounds__(kResThreads, 1)
         uint8_t* stage = sStage + warp * kStageWarp;
         // epilogue of tile pt: normalized bf16 partial rows (row pk >> 3, slot
         // pk & 7 of head pti.bh) and their log2-sum-exp
-        auto epilogue = [&](int pt, const ResTile& pti, int pk, float pl, float pm) -> bool {
+        // plt: the whole row sum when the two halves already exchanged it (with the
+        // next tile's first row maxima), else < 0 and the epilogue exchanges it
+        auto epilogue = [&](int pt, const ResTile& pti, int pk, float pl, float pm, float plt) -> bool {
             constexpr int PPR = DH / 8, RPI = 32 / PPR;  // pieces per half row, rows per store instruction
             const int ob = pt & 1;
             if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (pt >> 1) & 1, status, abort_v))) return false;
@@ -1917,13 +1919,19 @@ __global__ void __launch_bounds__(kResThreads, 1)
 #pragma unroll
             for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(tO + c0, o + c0);
             tmem_wait_ld();
-            xl[pt & 1][wg][r] = pl;
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ebar[pt & 1]);
-            if (!__all_sync(0xffffffffu, ws_wait(&ebar[pt & 1], (pt >> 1) & 1, status, abort_v))) return false;
+            float lt = plt;
+            if (plt < 0.0f) {  // the CTA's last tile: one exchange of its own (ebar's only use)
+                xl[pt & 1][wg][r] = pl;
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ebar[0]);
+                if (!__all_sync(0xffffffffu, ws_wait(&ebar[0], 0, status, abort_v))) return false;
+                lt = pl + xl[pt & 1][wg ^ 1][r];
+            } else {
+                fence_before_sync();
+                __syncwarp();
+            }
             if (lane == 0) mbar_arrive(&o_free[ob]);
-            const float lt = pl + xl[pt & 1][wg ^ 1][r];
             const float inv = pk >= 0 ? 1.0f / lt : 0.0f;
             const size_t pr = pk >= 0 ? ((size_t)pti.bh * N + (pk >> 3)) * s + (pk & 7) : 0;
 #pragma unroll
@@ -1990,6 +1998,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                     for (int j = 0; j < 64; ++j) mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
                 }
                 xmax[g & 1][wg][r] = mx;
+                if (c == 0 && have_prev) xl[(tl - 1) & 1][wg][r] = pl;  // the previous tile's row-sum half
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&xbar[g & 1]);
@@ -2048,7 +2057,8 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 if (lane == 0) mbar_arrive(&p_full[g & 1]);
                 // the previous tile's epilogue, now that its last O += P V has had a chunk's time
                 if (c == 0 && have_prev) {
-                    if (!(ok = epilogue(tl - 1, pti, ppk, pl, pm))) break;
+                    // the other half posted its share before this chunk's exchange
+                    if (!(ok = epilogue(tl - 1, pti, ppk, pl, pm, pl + xl[(tl - 1) & 1][wg ^ 1][r]))) break;
                     have_prev = false;
                 }
             }
@@ -2060,7 +2070,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
             pl = l;
             pm = mref;
         }
-        if (ok && have_prev) epilogue(nloc - 1, pti, ppk, pl, pm);
+        if (ok && have_prev) epilogue(nloc - 1, pti, ppk, pl, pm, -1.0f);
     }
     fence_before_sync();
     __syncthreads();
