@@ -754,7 +754,7 @@ __global__ void __launch_bounds__(320, 1)
     __shared__ uint64_t q_full[NSQ], q_empty[NSQ], r_full[2], p_full[2], o_full[2], o_free[2];
     __shared__ uint64_t lm_full, lm_free, xbar, ebar, kbar;  // lm_free: the MMA warp is done with a head's landmarks
     __shared__ int qgen[NSQ];  // landmark load each query tile uses (1-based)
-    __shared__ float xmax[2][2][kT], xl[2][kT];  // xmax[tile parity][half][row]
+    __shared__ float xmax[2][2][kT], xl[2][2][kT];  // [tile parity][half][row]
     __shared__ uint32_t xkey[kT][SMAX];  // the second half's s best, handed to the first
     __shared__ int xidx[kT][SMAX];
     __shared__ uint32_t tmem_slot;
@@ -887,7 +887,9 @@ __global__ void __launch_bounds__(320, 1)
         // next tile's scores, so its P Vt has had that long to finish
         const int wg = warp >> 2, r = threadIdx.x & 127;
         uint8_t* stage = sStage + warp * kStageWarp;
-        auto epilogue = [&](int pt, float lsum, float mx) -> bool {
+        // lt: the whole row sum when the halves already exchanged it (with the next
+        // tile's row maxima), else < 0 and the epilogue exchanges it (last tile)
+        auto epilogue = [&](int pt, float lsum, float mx, float lt) -> bool {
             constexpr int PPR = DH / 8, RPI = 32 / PPR;  // pieces per half row, rows per store instruction
             const int ob = pt & 1;
             const int bh = head(pt), q0 = ((t_begin + pt) % tiles_per_head) * kT, q = q0 + r;
@@ -898,15 +900,17 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(lane_base(tmem) + kO0 + ob * D + wg * DH + c0, o + c0);
             tmem_wait_ld();
-            xl[wg][r] = lsum;
+            if (lt < 0.0f) xl[pt & 1][wg][r] = lsum;
             fence_before_sync();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&o_free[ob]);
-                mbar_arrive(&ebar);
+                if (lt < 0.0f) mbar_arrive(&ebar);
             }
-            if (!__all_sync(0xffffffffu, ws_wait(&ebar, pt & 1, status, abort_v))) return false;
-            const float lt = lsum + xl[wg ^ 1][r];
+            if (lt < 0.0f) {  // ebar's only use
+                if (!__all_sync(0xffffffffu, ws_wait(&ebar, 0, status, abort_v))) return false;
+                lt = lsum + xl[pt & 1][wg ^ 1][r];
+            }
             const float inv = 1.0f / lt;
             const size_t row0 = (size_t)bh * N + q0 + (r & ~31);  // this warp's first row
 #pragma unroll
@@ -960,6 +964,7 @@ __global__ void __launch_bounds__(320, 1)
                 for (int j = 0; j < 64; ++j) mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
             }
             xmax[tl & 1][wg][r] = mx;
+            if (tl > 0) xl[(tl - 1) & 1][wg][r] = plsum;  // the previous tile's row-sum half
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&xbar);
@@ -1007,11 +1012,12 @@ __global__ void __launch_bounds__(320, 1)
                 }
             }
             if (threadIdx.x == 0) MITA_TRACE_EV(2, 23);
-            if (tl > 0 && !(ok = epilogue(tl - 1, plsum, pmx))) break;
+            // the other half posted its share before this tile's exchange
+            if (tl > 0 && !(ok = epilogue(tl - 1, plsum, pmx, plsum + xl[(tl - 1) & 1][wg ^ 1][r]))) break;
             plsum = lsum;
             pmx = mx;
         }
-        if (ok && nloc > 0) epilogue(nloc - 1, plsum, pmx);
+        if (ok && nloc > 0) epilogue(nloc - 1, plsum, pmx, -1.0f);
     }
     fence_before_sync();
     __syncthreads();
