@@ -30,9 +30,9 @@ METRIC = "MiTA fwd query-tokens/sec·head and % roofline at N=32k bf16, 1×GB300
 UNIT = "query-tokens/s·head"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dram__bytes_read.sum + dram__bytes_write.sum of one expert-attention launch
-# (k_expert_res) on the 32k long-context workload: a 6-head capture (157.3 MB)
+# (k_expert_res) on the 32k long-context workload: a 6-head capture (157.9 MB)
 # scaled by 32 / 6 heads (profiles/k_expert_res_longctx_6heads.md).
-EXPERT_TRAFFIC_BYTES = 8.39e8
+EXPERT_TRAFFIC_BYTES = 8.42e8
 
 
 def peaks():
