@@ -122,13 +122,20 @@ __device__ __forceinline__ float key_float(uint32_t v) {
 // lowered by a small margin, is a threshold that at least k keys of the full
 // row reach, so every top-k key of the row scores at or above it.
 __global__ void __launch_bounds__(512) k_sample_threshold(const float* __restrict__ Ssamp, int n_samp, int k,
-                                                          float* __restrict__ thr) {
+                                                          float* __restrict__ thr, int staged) {
+    extern __shared__ uint32_t skeys[];  // the row's order keys when staged
     __shared__ unsigned hist[256];
     const size_t row = blockIdx.x;
     const float* s = Ssamp + row * n_samp;
     uint32_t v;
     int rem;
-    radix_kth(n_samp, k, [&](int j) { return order_key(s[j]); }, hist, &v, &rem);
+    if (staged) {  // one coalesced read of the row; the radix passes run in shared memory
+        for (int j = threadIdx.x; j < n_samp; j += blockDim.x) skeys[j] = order_key(s[j]);
+        __syncthreads();
+        radix_kth(n_samp, k, [&](int j) { return skeys[j]; }, hist, &v, &rem);
+    } else {
+        radix_kth(n_samp, k, [&](int j) { return order_key(s[j]); }, hist, &v, &rem);
+    }
     if (threadIdx.x == 0) {
         const float t = key_float(v);
         thr[row] = t - 1e-3f * fmaxf(1.0f, fabsf(t));
@@ -303,7 +310,13 @@ __global__ void __launch_bounds__(512) k_topk_cand(const int2* __restrict__ cand
 
 cudaError_t launch_sample_threshold(const float* Ssamp, long long rows, int n_samp, int k, float* thr,
                                     cudaStream_t st) {
-    k_sample_threshold<<<(unsigned)rows, 512, 0, st>>>(Ssamp, n_samp, k, thr);
+    const int bytes = n_samp * 4;
+    const int staged = bytes <= 96 * 1024;
+    if (staged) {
+        cudaError_t e0 = cudaFuncSetAttribute(k_sample_threshold, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e0 != cudaSuccess) return e0;
+    }
+    k_sample_threshold<<<(unsigned)rows, 512, staged ? bytes : 0, st>>>(Ssamp, n_samp, k, thr, staged);
     count_launch();
     return cudaGetLastError();
 }
