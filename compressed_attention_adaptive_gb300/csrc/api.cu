@@ -87,7 +87,7 @@ static mita_status resolve(const mita_params* p, Dims* D) {
     D->flags = p->flags;
     D->dtype = p->dtype;
     D->shared = !(p->flags & MITA_FLAG_NO_SHARED);
-    if (out_simt_smem(*D) > 200 * 1024) return fail(MITA_ERR_UNSUPPORTED, "m + s*k too large for this build");
+    if (out_simt_smem(*D) > 200 * 1024) return fail(MITA_ERR_UNSUPPORTED, "m + s*k too large for this library");
     return MITA_OK;
 }
 

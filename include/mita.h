@@ -50,7 +50,7 @@ extern "C" {
 typedef enum {
     MITA_OK = 0,
     MITA_ERR_INVALID_ARG = 1, /* bad shape, pointer, flag or dtype             */
-    MITA_ERR_UNSUPPORTED = 2, /* valid MiTA parameters this build cannot run   */
+    MITA_ERR_UNSUPPORTED = 2, /* valid MiTA parameters this library cannot run */
     MITA_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or too small       */
     MITA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed          */
     MITA_ERR_TIMEOUT = 5,     /* device: a bounded wait gave up                */

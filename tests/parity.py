@@ -1,6 +1,6 @@
 """Parity checks of the CUDA path against the fp64 oracle.
 
-The rules (expert sets, routes, outputs) are those the build fixes for the
+The parity rules (expert sets, routes, outputs) for the
 MiTA forward pass:
 
 * Expert sets I_i: if the oracle's k-th and (k+1)-th raw scores differ by more
