@@ -123,7 +123,6 @@ def test_full_n131k():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["sweep_m32_k64_s1", "sweep_m128_k256_s2", "sweep_m512_k1024_s4",
-                                  "sweep_m512_k64_s4", "sweep_m32_k1024_s1"])
+@pytest.mark.parametrize("name", [w.name for w in synth.sweep_workloads()])
 def test_full_sweep_points(name):
     _full(synth.get(name), heads=[7])
