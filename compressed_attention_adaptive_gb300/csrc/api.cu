@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <string>
@@ -184,10 +185,11 @@ static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 static mita_status run(const mita_params* p, const void* Q, const void* K, const void* V, void* O, float* Qt_out,
                        int32_t* idx_out, int32_t* route_out, float* Vt_out, void* ws, size_t ws_bytes,
-                       void* stream, int upto) {
+                       void* stream, int upto, bool keep_status = false) {
     Dims D;
     mita_status st = resolve(p, &D);
     if (st) return st;
+    if (keep_status) D.flags |= kFlagKeepStatus;
     if (!Q || !aligned16(Q)) return fail(MITA_ERR_INVALID_ARG, "Q must be a 16-byte aligned device pointer");
     if (upto >= 1 && (!K || !aligned16(K))) return fail(MITA_ERR_INVALID_ARG, "K must be a 16-byte aligned device pointer");
     if (upto >= 2 && (!V || !aligned16(V))) return fail(MITA_ERR_INVALID_ARG, "V must be a 16-byte aligned device pointer");
@@ -281,6 +283,23 @@ size_t mita_host_buffer_size(const mita_params* p) {
     return 4 * t + mita_workspace_size(p);
 }
 
+// Streams and events of one mita_forward_host call; released when the call
+// returns (the runtime frees them once the work queued on them is done).
+struct HostPipe {
+    cudaStream_t in = nullptr, out = nullptr;
+    std::vector<cudaEvent_t> ev;
+    ~HostPipe() {
+        for (cudaEvent_t e : ev) cudaEventDestroy(e);
+        if (in) cudaStreamDestroy(in);
+        if (out) cudaStreamDestroy(out);
+    }
+    cudaError_t event(cudaEvent_t* e) {
+        cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
+        if (r == cudaSuccess) ev.push_back(*e);
+        return r;
+    }
+};
+
 mita_status mita_forward_host(const mita_params* p, const void* Q, const void* K, const void* V, void* O, void* dev,
                               size_t dev_bytes, void* stream) {
     g_last_error.clear();
@@ -291,17 +310,52 @@ mita_status mita_forward_host(const mita_params* p, const void* Q, const void* K
     const size_t need = mita_host_buffer_size(p);
     if (!dev || (uintptr_t)dev % 256) return fail(MITA_ERR_WORKSPACE, "device buffer NULL or not 256-byte aligned");
     if (dev_bytes < need) return fail(MITA_ERR_WORKSPACE, "device buffer too small: %zu < %zu bytes", dev_bytes, need);
-    const size_t bytes = (size_t)D.BH * D.N * D.d * elem_size(D);
-    const size_t t = align_up(bytes, 1024);
+    const size_t head = (size_t)D.N * D.d * elem_size(D);  // bytes of one head of Q, K, V or O
+    const size_t t = align_up((size_t)D.BH * head, 1024);
     char* b = (char*)dev;
+    const char *hq = (const char*)Q, *hk = (const char*)K, *hv = (const char*)V;
+    char* ho = (char*)O;
     cudaStream_t s = (cudaStream_t)stream;
-    MITA_CUDA(cudaMemcpyAsync(b, Q, bytes, cudaMemcpyHostToDevice, s), "copy Q to device");
-    MITA_CUDA(cudaMemcpyAsync(b + t, K, bytes, cudaMemcpyHostToDevice, s), "copy K to device");
-    MITA_CUDA(cudaMemcpyAsync(b + 2 * t, V, bytes, cudaMemcpyHostToDevice, s), "copy V to device");
-    st = run(p, b, b + t, b + 2 * t, b + 3 * t, nullptr, nullptr, nullptr, nullptr, b + 4 * t, dev_bytes - 4 * t,
-             stream, 2);
-    if (st) return st;
-    MITA_CUDA(cudaMemcpyAsync(O, b + 3 * t, bytes, cudaMemcpyDeviceToHost, s), "copy O to host");
+    // Heads are independent and contiguous in [B, H, N, d]: in groups of heads,
+    // group g + 1's inputs go in and group g - 1's output comes out (two copy
+    // streams) while group g computes on `stream`; the copy streams join
+    // `stream` at the end, so the call stays ordered on it.
+    const int G = head % 256 ? 1 : std::min(D.BH, 4);
+    const int hb = (D.BH + G - 1) / G;
+    HostPipe hp;
+    cudaEvent_t e0;
+    MITA_CUDA(cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking), "create copy stream");
+    MITA_CUDA(cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking), "create copy stream");
+    MITA_CUDA(hp.event(&e0), "create event");
+    MITA_CUDA(cudaEventRecord(e0, s), "record event");  // earlier work on `stream` first
+    MITA_CUDA(cudaStreamWaitEvent(hp.in, e0, 0), "order copies");
+    MITA_CUDA(cudaStreamWaitEvent(hp.out, e0, 0), "order copies");
+    for (int g = 0; g < G; ++g) {
+        const int h0 = g * hb, nh = std::min(hb, D.BH - h0);
+        if (nh <= 0) break;
+        const size_t off = (size_t)h0 * head, len = (size_t)nh * head;
+        cudaEvent_t ein, erun;
+        MITA_CUDA(cudaMemcpyAsync(b + off, hq + off, len, cudaMemcpyHostToDevice, hp.in), "copy Q to device");
+        MITA_CUDA(cudaMemcpyAsync(b + t + off, hk + off, len, cudaMemcpyHostToDevice, hp.in), "copy K to device");
+        MITA_CUDA(cudaMemcpyAsync(b + 2 * t + off, hv + off, len, cudaMemcpyHostToDevice, hp.in), "copy V to device");
+        MITA_CUDA(hp.event(&ein), "create event");
+        MITA_CUDA(cudaEventRecord(ein, hp.in), "record event");
+        MITA_CUDA(cudaStreamWaitEvent(s, ein, 0), "order compute after copies");
+        mita_params pg = *p;  // heads h0 .. h0 + nh - 1 as one batch of nh heads
+        pg.B = 1;
+        pg.H = nh;
+        st = run(&pg, b + off, b + t + off, b + 2 * t + off, b + 3 * t + off, nullptr, nullptr, nullptr, nullptr,
+                 b + 4 * t, dev_bytes - 4 * t, stream, 2, g > 0);
+        if (st) return st;
+        MITA_CUDA(hp.event(&erun), "create event");
+        MITA_CUDA(cudaEventRecord(erun, s), "record event");
+        MITA_CUDA(cudaStreamWaitEvent(hp.out, erun, 0), "order copy after compute");
+        MITA_CUDA(cudaMemcpyAsync(ho + off, b + 3 * t + off, len, cudaMemcpyDeviceToHost, hp.out), "copy O to host");
+    }
+    cudaEvent_t eend;
+    MITA_CUDA(hp.event(&eend), "create event");
+    MITA_CUDA(cudaEventRecord(eend, hp.out), "record event");
+    MITA_CUDA(cudaStreamWaitEvent(s, eend, 0), "join copy stream");
     return MITA_OK;
 }
 

@@ -11,6 +11,10 @@ namespace mita {
 // Device status codes (mirror mita_status).
 enum : int { kStOk = 0, kStTimeout = 5, kStBounds = 6 };
 
+// Internal flag bit in Dims::flags (never a public MITA_FLAG_*): the call is
+// one part of a larger one, so its first kernel keeps the device status word.
+constexpr unsigned kFlagKeepStatus = 1u << 31;
+
 // Problem dimensions after validation (1-D pooling is a 1 x N grid).
 struct Dims {
     int B, H, BH, N, d, m, k, s;

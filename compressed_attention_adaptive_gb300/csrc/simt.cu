@@ -26,8 +26,9 @@ __global__ void __launch_bounds__(256) k_pool(const T* __restrict__ Q, float* __
                                               int m_pad, Dims D, int* __restrict__ status) {
     __shared__ float red[256 * 8];
     const int i = blockIdx.x, bh = blockIdx.y, d = D.d;
-    // the first kernel of every call resets the device status word
-    if (status && i == 0 && bh == 0 && threadIdx.x == 0) *status = kStOk;
+    // the first kernel of every call resets the device status word (not in the
+    // later parts of a call split into several)
+    if (status && !(D.flags & kFlagKeepStatus) && i == 0 && bh == 0 && threadIdx.x == 0) *status = kStOk;
     const int ncg = d >> 3, nlanes = 256 / ncg;
     const int cg = threadIdx.x % ncg, tl = threadIdx.x / ncg;
     float acc[8];

@@ -108,9 +108,13 @@ size_t mita_host_buffer_size(const mita_params* p);
 /* The forward pass on HOST buffers: Q, K, V, O are host pointers (pinned
  * memory gives full copy speed), `dev` is caller-owned device memory of at
  * least mita_host_buffer_size() bytes. Copies Q, K, V to the device, runs the
- * forward pass, copies O back, all enqueued on `stream`; the call returns
- * without waiting, so the host buffers must stay valid until the stream has
- * passed the copies. */
+ * forward pass, copies O back. The heads are processed in a few groups so that
+ * one group's copies overlap another's compute: the copies run on two streams
+ * the call creates and releases, ordered after earlier work on `stream` and
+ * joined back into it, so all of the call's work is ordered on `stream`. The
+ * call returns without waiting; the host buffers must stay valid until
+ * `stream` has passed it. The device status word is the workspace's, at
+ * offset 4 * align_up(B*H*N*d*element size, 1024) bytes of `dev`. */
 mita_status mita_forward_host(const mita_params* p, const void* Q, const void* K, const void* V, void* O,
                               void* dev, size_t dev_bytes, void* stream);
 
