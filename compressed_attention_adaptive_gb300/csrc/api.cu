@@ -320,7 +320,7 @@ mita_status mita_forward_host(const mita_params* p, const void* Q, const void* K
     // group g + 1's inputs go in and group g - 1's output comes out (two copy
     // streams) while group g computes on `stream`; the copy streams join
     // `stream` at the end, so the call stays ordered on it.
-    const int G = head % 256 ? 1 : std::min(D.BH, 4);
+    const int G = head % 256 ? 1 : std::min(D.BH, 8);
     const int hb = (D.BH + G - 1) / G;
     HostPipe hp;
     cudaEvent_t e0;

@@ -2106,6 +2106,7 @@ TcPlan tc_plan(const Dims& D) {
     const long long target = 4LL * 148;
     long long sp = (target + (long long)D.BH * p.m_tiles - 1) / ((long long)D.BH * p.m_tiles);
     if (sp < 1) sp = 1;
+    if (sp > 128) sp = 128;  // <= 256 candidate regions per row (two column halves per split) stay stageable
     if (sp > nchunks) sp = nchunks;
     p.chunks_per_split = (int)((nchunks + sp - 1) / sp);
     p.splits = (nchunks + p.chunks_per_split - 1) / p.chunks_per_split;
