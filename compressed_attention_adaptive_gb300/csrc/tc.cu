@@ -130,14 +130,6 @@ __device__ __forceinline__ void issue_pv_ts(uint32_t tO, uint32_t tP, uint32_t s
         mma_bf16_ts(tO, tP + kk * 8, sdesc(sV + kk * 2048, kT * 128, 1024), id, (kk > 0 || accumulate) ? 1u : 0u);
 }
 
-// This thread's 128 probabilities, bf16 packed two per column, into TMEM
-// columns tP .. tP + 63 of its lane (warp-collective).
-__device__ __forceinline__ void tmem_store_p(uint32_t tP, const uint32_t (&pk)[64]) {
-    tmem_st32(tP, reinterpret_cast<const float*>(pk));
-    tmem_st32(tP + 32, reinterpret_cast<const float*>(pk + 32));
-    tmem_wait_st();
-}
-
 // Copies an R-row operand tile (R a multiple of 8): row t comes from
 // src_row(t) (nullptr -> zero row), D bf16 per row, into the swizzled layout
 // at sbase. src_row(-1) must return any valid global address.
