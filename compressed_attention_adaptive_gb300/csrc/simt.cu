@@ -43,23 +43,41 @@ __global__ void __launch_bounds__(256) k_pool(const T* __restrict__ Q, float* __
         cnt = (r1 - r0) * nc;
         if (tl < nlanes) {
             const T* base = Q + (size_t)bh * D.N * d + cg * 8;
-            for (int t = tl; t < cnt; t += nlanes) {
-                const size_t tok = (size_t)(r0 + t / nc) * D.gw + (c0 + t % nc);
-                const T* p = base + tok * d;
-                if constexpr (sizeof(T) == 2) {
-                    uint4 v = *reinterpret_cast<const uint4*>(p);
-                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+            // token t of the bin is (row r0 + t / nc, column c0 + t % nc); the
+            // lane walks t = tl, tl + nlanes, ... keeping (row, column) by steps,
+            // four tokens' loads in flight before their sums
+            int r = tl / nc, c = tl % nc;
+            for (int t = tl; t < cnt; t += 4 * nlanes) {
+                uint4 v[4][sizeof(T) / 2];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        float2 f = __bfloat1622float2(b2[j]);
-                        acc[2 * j] += f.x;
-                        acc[2 * j + 1] += f.y;
+                for (int u = 0; u < 4; ++u) {
+                    if (t + u * nlanes < cnt) {
+                        const T* p = base + ((size_t)(r0 + r) * D.gw + (c0 + c)) * d;
+#pragma unroll
+                        for (int w = 0; w < (int)(sizeof(T) / 2); ++w) v[u][w] = reinterpret_cast<const uint4*>(p)[w];
                     }
-                } else {
-                    float4 a = *reinterpret_cast<const float4*>(p);
-                    float4 b = *reinterpret_cast<const float4*>(p + 4);
-                    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-                    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+                    c += nlanes;
+                    while (c >= nc) {
+                        c -= nc;
+                        ++r;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (t + u * nlanes >= cnt) break;
+                    if constexpr (sizeof(T) == 2) {
+                        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&v[u][0]);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float2 f = __bfloat1622float2(b2[j]);
+                            acc[2 * j] += f.x;
+                            acc[2 * j + 1] += f.y;
+                        }
+                    } else {
+                        const float* f = reinterpret_cast<const float*>(&v[u][0]);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[j] += f[j];
+                    }
                 }
             }
         }
