@@ -283,22 +283,33 @@ size_t mita_host_buffer_size(const mita_params* p) {
     return 4 * t + mita_workspace_size(p);
 }
 
-// Streams and events of one mita_forward_host call; released when the call
-// returns (the runtime frees them once the work queued on them is done).
+// Copy streams and events of mita_forward_host, created once per device and
+// kept for the process (creating them on every call costs host time in the
+// middle of a pipelined sequence of calls). g_host_mu serializes the enqueue
+// sequences, so that no two calls record the same event concurrently.
+constexpr int kHostGroups = 8;
 struct HostPipe {
     cudaStream_t in = nullptr, out = nullptr;
-    std::vector<cudaEvent_t> ev;
-    ~HostPipe() {
-        for (cudaEvent_t e : ev) cudaEventDestroy(e);
-        if (in) cudaStreamDestroy(in);
-        if (out) cudaStreamDestroy(out);
-    }
-    cudaError_t event(cudaEvent_t* e) {
-        cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
-        if (r == cudaSuccess) ev.push_back(*e);
-        return r;
-    }
+    cudaEvent_t ev[2 * kHostGroups + 2] = {};
 };
+static std::mutex g_host_mu;
+static HostPipe g_host_pipe[64];
+
+static cudaError_t host_pipe(HostPipe** hp) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    HostPipe& h = g_host_pipe[dev];
+    if (!h.in) {
+        if ((e = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        for (cudaEvent_t& x : h.ev)
+            if ((e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *hp = &h;
+    return cudaSuccess;
+}
 
 mita_status mita_forward_host(const mita_params* p, const void* Q, const void* K, const void* V, void* O, void* dev,
                               size_t dev_bytes, void* stream) {
@@ -318,28 +329,27 @@ mita_status mita_forward_host(const mita_params* p, const void* Q, const void* K
     cudaStream_t s = (cudaStream_t)stream;
     // Heads are independent and contiguous in [B, H, N, d]: in groups of heads,
     // group g + 1's inputs go in and group g - 1's output comes out (two copy
-    // streams) while group g computes on `stream`; the copy streams join
-    // `stream` at the end, so the call stays ordered on it.
-    const int G = head % 256 ? 1 : std::min(D.BH, 8);
+    // streams) while group g computes on `stream`; the copy streams wait for
+    // earlier work on `stream` and join it at the end, so the call stays
+    // ordered on it.
+    const int G = head % 256 ? 1 : std::min(D.BH, kHostGroups);
     const int hb = (D.BH + G - 1) / G;
-    HostPipe hp;
-    cudaEvent_t e0;
-    MITA_CUDA(cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking), "create copy stream");
-    MITA_CUDA(cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking), "create copy stream");
-    MITA_CUDA(hp.event(&e0), "create event");
-    MITA_CUDA(cudaEventRecord(e0, s), "record event");  // earlier work on `stream` first
-    MITA_CUDA(cudaStreamWaitEvent(hp.in, e0, 0), "order copies");
-    MITA_CUDA(cudaStreamWaitEvent(hp.out, e0, 0), "order copies");
+    std::lock_guard<std::mutex> lk(g_host_mu);
+    HostPipe* hp = nullptr;
+    MITA_CUDA(host_pipe(&hp), "create copy streams");
+    cudaEvent_t* ev = hp->ev;
+    MITA_CUDA(cudaEventRecord(ev[0], s), "record event");  // earlier work on `stream` first
+    MITA_CUDA(cudaStreamWaitEvent(hp->in, ev[0], 0), "order copies");
+    MITA_CUDA(cudaStreamWaitEvent(hp->out, ev[0], 0), "order copies");
     for (int g = 0; g < G; ++g) {
         const int h0 = g * hb, nh = std::min(hb, D.BH - h0);
         if (nh <= 0) break;
         const size_t off = (size_t)h0 * head, len = (size_t)nh * head;
-        cudaEvent_t ein, erun;
-        MITA_CUDA(cudaMemcpyAsync(b + off, hq + off, len, cudaMemcpyHostToDevice, hp.in), "copy Q to device");
-        MITA_CUDA(cudaMemcpyAsync(b + t + off, hk + off, len, cudaMemcpyHostToDevice, hp.in), "copy K to device");
-        MITA_CUDA(cudaMemcpyAsync(b + 2 * t + off, hv + off, len, cudaMemcpyHostToDevice, hp.in), "copy V to device");
-        MITA_CUDA(hp.event(&ein), "create event");
-        MITA_CUDA(cudaEventRecord(ein, hp.in), "record event");
+        cudaEvent_t ein = ev[1 + 2 * g], erun = ev[2 + 2 * g];
+        MITA_CUDA(cudaMemcpyAsync(b + off, hq + off, len, cudaMemcpyHostToDevice, hp->in), "copy Q to device");
+        MITA_CUDA(cudaMemcpyAsync(b + t + off, hk + off, len, cudaMemcpyHostToDevice, hp->in), "copy K to device");
+        MITA_CUDA(cudaMemcpyAsync(b + 2 * t + off, hv + off, len, cudaMemcpyHostToDevice, hp->in), "copy V to device");
+        MITA_CUDA(cudaEventRecord(ein, hp->in), "record event");
         MITA_CUDA(cudaStreamWaitEvent(s, ein, 0), "order compute after copies");
         mita_params pg = *p;  // heads h0 .. h0 + nh - 1 as one batch of nh heads
         pg.B = 1;
@@ -347,15 +357,12 @@ mita_status mita_forward_host(const mita_params* p, const void* Q, const void* K
         st = run(&pg, b + off, b + t + off, b + 2 * t + off, b + 3 * t + off, nullptr, nullptr, nullptr, nullptr,
                  b + 4 * t, dev_bytes - 4 * t, stream, 2, g > 0);
         if (st) return st;
-        MITA_CUDA(hp.event(&erun), "create event");
         MITA_CUDA(cudaEventRecord(erun, s), "record event");
-        MITA_CUDA(cudaStreamWaitEvent(hp.out, erun, 0), "order copy after compute");
-        MITA_CUDA(cudaMemcpyAsync(ho + off, b + 3 * t + off, len, cudaMemcpyDeviceToHost, hp.out), "copy O to host");
+        MITA_CUDA(cudaStreamWaitEvent(hp->out, erun, 0), "order copy after compute");
+        MITA_CUDA(cudaMemcpyAsync(ho + off, b + 3 * t + off, len, cudaMemcpyDeviceToHost, hp->out), "copy O to host");
     }
-    cudaEvent_t eend;
-    MITA_CUDA(hp.event(&eend), "create event");
-    MITA_CUDA(cudaEventRecord(eend, hp.out), "record event");
-    MITA_CUDA(cudaStreamWaitEvent(s, eend, 0), "join copy stream");
+    MITA_CUDA(cudaEventRecord(ev[2 * kHostGroups + 1], hp->out), "record event");
+    MITA_CUDA(cudaStreamWaitEvent(s, ev[2 * kHostGroups + 1], 0), "join copy stream");
     return MITA_OK;
 }
 

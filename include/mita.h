@@ -110,8 +110,9 @@ size_t mita_host_buffer_size(const mita_params* p);
  * least mita_host_buffer_size() bytes. Copies Q, K, V to the device, runs the
  * forward pass, copies O back. The heads are processed in a few groups so that
  * one group's copies overlap another's compute: the copies run on two streams
- * the call creates and releases, ordered after earlier work on `stream` and
- * joined back into it, so all of the call's work is ordered on `stream`. The
+ * the library keeps per device, ordered after earlier work on `stream` and
+ * joined back into it, so all of the call's work is ordered on `stream`
+ * (concurrent calls from several host threads enqueue one after another). The
  * call returns without waiting; the host buffers must stay valid until
  * `stream` has passed it. The device status word is the workspace's, at
  * offset 4 * align_up(B*H*N*d*element size, 1024) bytes of `dev`. */
