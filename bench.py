@@ -29,10 +29,12 @@ sys.path.insert(0, ROOT)
 METRIC = "MiTA fwd query-tokens/sec·head and % roofline at N=32k bf16, 1×GB300"
 UNIT = "query-tokens/s·head"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# dram__bytes_read.sum + dram__bytes_write.sum of one expert-attention launch
-# (k_expert_res) on the 32k long-context workload: a 6-head capture (157.9 MB)
-# scaled by 32 / 6 heads (profiles/k_expert_res_longctx_6heads.md).
-EXPERT_TRAFFIC_BYTES = 8.42e8
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the dominant kernel on the 32k long-context workload, from an ncu capture of
+# a smaller head count scaled to 32 heads. It is tied to the kernel source it
+# was taken on (sha256 of csrc/tc.cu, first 16 hex digits); once that source
+# changes, the figure no longer describes the kernel and the line reports null.
+EXPERT_TRAFFIC = {"kernel": None, "tc_cu_sha16": None, "bytes_per_launch": None, "how": None}
 
 
 def peaks():
@@ -49,8 +51,38 @@ def work_counts(w):
     elem = 2 if w.dtype == "bf16" else 4
     F = 4.0 * w.BH * w.N * w.d * (2 * w.m + w.s * w.k)
     Bytes = 4.0 * w.BH * w.N * w.d * elem
-    expert_F = 4.0 * w.BH * w.N * w.d * (w.s * w.k + w.m)  # routed slots + shared slots
-    return F, Bytes, expert_F
+    return F, Bytes
+
+
+def expert_flops(w, with_shared):
+    """Algorithmic flops of one expert-attention launch: q . k and p . v over
+    the s * k routed slots of every query (plus the m shared slots when the
+    kernel computes those too)."""
+    return 4.0 * w.BH * w.N * w.d * (w.s * w.k + (w.m if with_shared else 0))
+
+
+def tc_cu_sha16():
+    import hashlib
+    with open(os.path.join(ROOT, "compressed_attention_adaptive_gb300", "csrc", "tc.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 class ClockSampler:
@@ -119,52 +151,130 @@ def job_max(dist, x):
     return float(t.item())
 
 
-def oracle_sample(w, n_heads, q_stride, threads, seed=0):
-    """Times the fp64 oracle on n_heads heads (one per thread), every
-    q_stride-th query. Returns (seconds, query-tokens*heads processed)."""
-    import numpy as np
-    import oracle
-    from compressed_attention_adaptive_gb300 import synth
-    heads = list(range(n_heads))
-    Qn, Kn, Vn = synth.make_inputs(w, seed=seed, heads=heads)
-    f = lambda a: synth.widen(a, w.dtype)
-    Q, K, V = f(Qn), f(Kn), f(Vn)
-    q_ids = None if q_stride == 1 else np.arange(0, w.N, q_stride)
-    t0 = time.perf_counter()
-    oracle.forward(Q, K, V, w.m, w.k, w.s, grid=w.grid, lm=w.lm, q_ids=q_ids, threads=threads)
-    dt = time.perf_counter() - t0
-    nq = w.N if q_ids is None else len(q_ids)
-    return dt, n_heads * nq
+class OracleSample:
+    """The fp64 oracle (unchanged, one head per host thread) on a bounded
+    sample of a workload: n_heads heads. The inputs are generated once, outside
+    every timed region."""
+
+    def __init__(self, w, n_heads, seed=0):
+        from compressed_attention_adaptive_gb300 import synth
+        Qn, Kn, Vn = synth.make_inputs(w, seed=seed, heads=list(range(n_heads)))
+        f = lambda a: synth.widen(a, w.dtype)
+        self.w, self.n_heads = w, n_heads
+        self.Q, self.K, self.V = f(Qn), f(Kn), f(Vn)
+
+    def run(self, q_ids=None, threads=None, heads=None):
+        """Seconds for the oracle forward on `heads` of the sample (all by
+        default), the queries q_ids (all if None) of each."""
+        import oracle
+        w = self.w
+        sl = slice(None) if heads is None else slice(0, heads)
+        t0 = time.perf_counter()
+        oracle.forward(self.Q[sl], self.K[sl], self.V[sl], w.m, w.k, w.s, grid=w.grid, lm=w.lm, q_ids=q_ids,
+                       threads=threads or self.n_heads)
+        return time.perf_counter() - t0
 
 
 def reference_arm(args, w, rank):
-    """The oracle timed as the reference implementation (rank 0 only)."""
+    """The oracle timed as the reference implementation (rank 0 only).
+
+    A step is `cores` whole heads (every query), one head per thread, when
+    (K + W) such steps fit in about four minutes. Otherwise a step is the same
+    heads at a stride of queries, and the per-head time of the whole workload
+    is assembled from two timed parts: the head's fixed work (a run with one
+    query: pooling, landmark pass, expert sets; timed once before the steps)
+    and the step's per-query work (its run minus the fixed part, per query),
+    so that the fixed part counts once per head as in the full workload, not
+    once per sampled block of queries."""
     if rank != 0:
         return
+    import numpy as np
     cores = os.cpu_count() or 1
     n_heads = min(w.BH, cores)
-    # per step about 150 s / (K + W), at least one landmark pass per head
-    budget = 150.0 / max(1, args.steps + args.warmup)
-    stride = 1
-    while stride < 64 and 2.5 + 8.6 / stride > budget:
-        stride *= 2
-    for _ in range(args.warmup):
-        oracle_sample(w, n_heads, stride, cores)
-    total_t, total_q = 0.0, 0
-    for _ in range(args.steps):
-        t, q = oracle_sample(w, n_heads, stride, cores)
-        total_t += t
-        total_q += q
-    value = total_q / total_t
-    sample = "%d of %d heads, every %d-th query (%d per head), %d threads, fp64 oracle" % (
-        n_heads, w.BH, stride, w.N // stride, cores)
+    S = OracleSample(w, n_heads)
+    t_full = S.run()  # calibration run (untimed in the line): one step of whole heads
+    steps = args.steps + args.warmup
+    if steps * t_full <= 240.0:
+        mode, stride = "whole heads", 1
+    else:
+        mode = "strided queries"
+        stride = 2
+        while stride < 4096 and steps * (0.2 * t_full + t_full / stride) > 150.0:
+            stride *= 2
+    q_sparse = np.arange(0, w.N, stride)
+    t_fixed = S.run(q_ids=np.array([0])) if mode != "whole heads" else 0.0  # calibration, untimed
+    total_t, est = 0.0, []
+    for i in range(steps):
+        if mode == "whole heads":
+            t = S.run()
+            per_head = t
+        else:
+            t = S.run(q_ids=q_sparse)
+            per_query = max(0.0, t - t_fixed) / max(1, len(q_sparse) - 1)
+            per_head = t_fixed + (w.N - 1) * per_query
+        if i >= args.warmup:
+            total_t += t
+            est.append(per_head)
+    per_head = sum(est) / len(est)  # wall seconds for n_heads whole heads on n_heads threads
+    value = n_heads * w.N / per_head
+    if mode == "whole heads":
+        sample = "%d of %d heads, all %d queries each, one head per thread (%d threads), fp64 oracle" % (
+            n_heads, w.BH, w.N, n_heads)
+    else:
+        sample = ("%d of %d heads, one head per thread (%d threads), fp64 oracle; per step one run with every "
+                  "%d-th query (%d per head); the whole-head time is the fixed per-head work (a run with one "
+                  "query per head, timed once before the steps) plus N - 1 times the per-query time each step "
+                  "measured") % (
+            n_heads, w.BH, n_heads, stride, len(q_sparse))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "m": w.m, "k": w.k, "s": w.s},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": n_heads, "kind": "oracle", "sample": sample,
+                             "cpu_model": cpu_model(), "host_cpus": cores},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w):
+    """The oracle on the host cores, bounded sample: `cores` whole heads, one
+    per thread; plus one head on one thread (the per-core rate)."""
+    cores = os.cpu_count() or 1
+    n_heads = min(w.BH, cores)
+    S = OracleSample(w, n_heads)
+    t = S.run()
+    t1 = S.run(heads=1, threads=1)
+    return {"value": n_heads * w.N / t, "unit": UNIT, "cores": n_heads, "kind": "oracle",
+            "sample": "%d of %d heads, all %d queries each, fp64 oracle, one head per thread" % (n_heads, w.BH, w.N),
+            "seconds": t, "cpu_model": cpu_model(), "host_cpus": cores,
+            "one_head_one_thread": {"seconds": t1, "value": w.N / t1, "unit": UNIT}}
+
+
+def expert_roofline(w, phase_ms, pk, pk_src, ms_step):
+    """Roofline of the dominant kernel, the expert attention: algorithmic
+    flops of one launch over its average duration (CUDA events recorded on the
+    launching stream around the launch, inside the timed region), against the
+    measured burst bf16 peak (the step is milliseconds long, not a sustained
+    seconds-long loop); the sustained peak is given beside it."""
+    resident = "merge" in phase_ms  # k_expert_res; the shared slots ran in the routing pass
+    flops = expert_flops(w, with_shared=not resident)
+    ms = phase_ms["expert"]
+    achieved = flops / (ms * 1e-3) / 1e12
+    kernel = "k_expert_res" if resident else "k_expert_ws"
+    traffic = None
+    if EXPERT_TRAFFIC["kernel"] == kernel and EXPERT_TRAFFIC["tc_cu_sha16"] == tc_cu_sha16() \
+            and w.name == "longctx_n32k":
+        traffic = EXPERT_TRAFFIC["bytes_per_launch"]
+    peak = pk["bf16_tflops"]
+    sus = pk.get("bf16_tflops_sustained")
+    return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": traffic,
+            "traffic_how": EXPERT_TRAFFIC["how"] if traffic else "no capture of the current kernel source",
+            "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % pk_src,
+            "frac_of_sustained": achieved / sus if sus else None,
+            "algorithmic_flops_per_launch": flops,
+            "flops_counted": "4*B*H*N*d*s*k (routed slots)" if resident else "4*B*H*N*d*(s*k+m) (routed + shared slots)",
+            "avg_launch_ms": ms, "share_of_step": ms / ms_step}
 
 
 def main():
@@ -240,30 +350,17 @@ def main():
     value = world * w.BH * w.N / (ms_step * 1e-3)
 
     pk, pk_src = peaks()
-    F, Bytes, expert_F = work_counts(w)
-    tensor_peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    F, Bytes = work_counts(w)
     t_roof = max(F / (pk["bf16_tflops"] * 1e12), Bytes / (pk["hbm_gbs"] * 1e9))
     phase_ms = {k: v / args.steps for k, v in phases.items()}
     uses_tc = mita.mita_uses_tensor_cores(p) == 1
-    dom = "expert" if "expert" in phase_ms else max(phase_ms, key=phase_ms.get)
-    dom_ms = phase_ms[dom]
-    achieved = expert_F / (dom_ms * 1e-3) / 1e12
-    kname = "k_expert_res (expert attention)" if "merge" in phase_ms else "k_expert_ws (expert attention + merge)"
-    roof = {"kernel": kname if dom == "expert" else dom,
-            "bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
-            "frac": achieved / tensor_peak,
-            "traffic": EXPERT_TRAFFIC_BYTES if (dom == "expert" and w.name == "longctx_n32k" and "merge" in phase_ms)
-            else None,
-            "peak_source": "%s bf16 sustained (MEASURED_PEAKS.json)" % pk_src,
-            "algorithmic_flops_per_launch": expert_F, "avg_launch_ms": dom_ms}
-
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "m": w.m, "k": w.k, "s": w.s,
                        "path": "tcgen05" if uses_tc else "cuda-core", "l2": "inputs larger than L2 (no flush)",
                        "parallelism": "replicas x%d" % world},
-            "roofline": roof,
+            "roofline": expert_roofline(w, phase_ms, pk, pk_src, ms_step) if "expert" in phase_ms else None,
             "path_roofline": {"t_roof_us": t_roof * 1e6, "frac": t_roof / (ms_step * 1e-3),
                               "flops": F, "compulsory_bytes": Bytes,
                               "peaks": {"bf16_tflops": pk["bf16_tflops"], "hbm_gbs": pk["hbm_gbs"],
@@ -271,14 +368,9 @@ def main():
             "phases_ms": phase_ms, "gpu_launches": launches, "clocks": clk}
 
     if not args.no_e2e:
-        line["e2e"] = e2e_run(mita, p, Qn, Kn, Vn, w, dev, min(args.steps, 10), dist, world)
+        line["e2e"] = e2e_run(mita, p, Qn, Kn, Vn, w, dev, max(30, min(args.steps, 50)), dist, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cores = os.cpu_count() or 1
-        n_heads = min(w.BH, cores)
-        t, q = oracle_sample(w, n_heads, 1, cores)
-        line["cpu_baseline"] = {"value": q / t, "unit": UNIT, "cores": min(cores, n_heads), "kind": "oracle",
-                                "sample": "%d of %d heads, all %d queries each, fp64 oracle, one head per thread"
-                                          % (n_heads, w.BH, w.N), "seconds": t}
+        line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -314,7 +406,7 @@ def sweep(args):
         torch.cuda.synchronize(dev)
         mita.mita_device_status(ws)
         ms = e0.elapsed_time(e1) / args.steps
-        F, Bytes, _ = work_counts(w)
+        F, Bytes = work_counts(w)
         t_f, t_b = F / (pk["bf16_tflops"] * 1e12), Bytes / (pk["hbm_gbs"] * 1e9)
         t_roof = max(t_f, t_b)
         print(json.dumps({"workload": name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "m": w.m, "k": w.k, "s": w.s,
@@ -326,30 +418,71 @@ def sweep(args):
         torch.cuda.empty_cache()
 
 
+def pinned_host(nbytes, torch):
+    """A page-locked host buffer (torch uint8 tensor) for the end-to-end run:
+    anonymous memory advised for transparent huge pages (fewer, larger pages
+    for the device's DMA engines to map), page-locked with cudaHostRegister;
+    torch's pin_memory() when that is unavailable."""
+    import mmap
+    try:
+        mm = mmap.mmap(-1, nbytes, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        if hasattr(mmap, "MADV_HUGEPAGE"):
+            mm.madvise(mmap.MADV_HUGEPAGE)
+        t = torch.frombuffer(mm, dtype=torch.uint8)
+        t.zero_()  # touch every page before registering
+        rc = torch.cuda.cudart().cudaHostRegister(t.data_ptr(), nbytes, 0)
+        if int(rc) != 0:
+            raise RuntimeError("cudaHostRegister failed: %s" % rc)
+        t._mita_mmap = mm  # keeps the mapping alive with the tensor
+        return t, "mmap+MADV_HUGEPAGE+cudaHostRegister"
+    except Exception:
+        return torch.empty(nbytes, dtype=torch.uint8).pin_memory(), "torch pin_memory"
+
+
 def e2e_run(mita, p, Qn, Kn, Vn, w, dev, steps, dist, world):
     """The same metric through mita_forward_host: pinned host buffers, copies
-    in, forward, copy out, all inside the timed region."""
+    in, forward, copy out, all inside the timed region. Per-step CUDA events
+    give the spread (median, min, max); the raw copy rate of the same buffers
+    is measured beside it."""
     import numpy as np
     import torch
-    hb = [torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8)).pin_memory() for a in (Qn, Kn, Vn)]
-    hO = torch.empty_like(hb[0]).pin_memory()
+    nbytes = Qn.nbytes
+    hb = []
+    for a in (Qn, Kn, Vn):
+        t, how = pinned_host(nbytes, torch)
+        t.copy_(torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8)))
+        hb.append(t)
+    hO, _ = pinned_host(nbytes, torch)
     buf = torch.empty(mita.mita_host_buffer_size(p), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    for _ in range(2):
+    for _ in range(3):
         mita.mita_forward_host(p, hb[0], hb[1], hb[2], hO, buf)
     torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
         mita.mita_forward_host(p, hb[0], hb[1], hb[2], hO, buf)
-    e1.record(stream)
+        ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
-    ms = job_max(dist, e0.elapsed_time(e1) / steps)
-    nbytes = hb[0].numel()
+    per = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+    ms = job_max(dist, ev[0].elapsed_time(ev[steps]) / steps)
+    # raw copy rates of the same pinned buffers (the floor of the end-to-end step)
+    c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    c0.record(stream)
+    for i in range(3):
+        buf[i * nbytes:(i + 1) * nbytes].copy_(hb[i], non_blocking=True)
+    c1.record(stream)
+    hO.copy_(buf[:nbytes], non_blocking=True)
+    c2.record(stream)
+    torch.cuda.synchronize(dev)
+    h2d_gbs = 3 * nbytes / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    d2h_gbs = nbytes / (c1.elapsed_time(c2) * 1e-3) / 1e9
     return {"value": world * w.BH * w.N / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": 3 * nbytes,
-            "d2h_bytes_per_step": nbytes, "ms_per_step": ms, "steps": steps}
+            "d2h_bytes_per_step": nbytes, "ms_per_step": ms, "steps": steps,
+            "ms_median": per[len(per) // 2], "ms_min": per[0], "ms_max": per[-1],
+            "host_buffers": how, "copy_only_h2d_gbs": h2d_gbs, "copy_only_d2h_gbs": d2h_gbs}
 
 
 if __name__ == "__main__":

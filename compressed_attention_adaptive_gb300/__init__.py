@@ -174,9 +174,12 @@ def mita_forward(p: Params, Q, K, V, O, ws, idx_out=None, route_out=None, Vt_out
 def mita_forward_static(p: Params, Q, K, V, O, status_out=None, stream=None):
     """The forward pass on the library's static device workspace (nothing is
     allocated): for callers that cannot allocate device memory. status_out is
-    an optional int32 device tensor receiving the device status word."""
-    _check(lib().mita_forward_static(ctypes.byref(p.c()), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(status_out),
-                                     _stream(stream)))
+    an optional int32 device tensor receiving the device status word. The
+    call runs with Q's device current (the static area is per device)."""
+    import torch
+    with torch.cuda.device(Q.device):
+        _check(lib().mita_forward_static(ctypes.byref(p.c()), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
+                                         _ptr(status_out), _stream(stream)))
 
 
 def mita_forward_host(p: Params, Q, K, V, O, dev, stream=None):

@@ -238,6 +238,8 @@ mita_status validate(const mita_params* p) {
 
 mita_status report_error(mita_status st, const char* msg) { return fail(st, "%s", msg); }
 
+void clear_error() { g_last_error.clear(); }
+
 mita_status forward_on_workspace(const mita_params* p, const void* Q, const void* K, const void* V, void* O,
                                  void* ws, size_t ws_bytes, void* stream) {
     return run(p, Q, K, V, O, nullptr, nullptr, nullptr, nullptr, ws, ws_bytes, stream, 2);

@@ -101,16 +101,4 @@ __host__ __device__ __forceinline__ void pool_bin(int i, int L, int P, int* lo, 
     *hi = (int)((((long long)(i + 1) * L) + P - 1) / P);
 }
 
-// Event trace of one CTA (block 0) for timing studies; compiled out unless
-// MITA_TRACE is defined (the trace buffers and trace_ev live in tc.cu).
-#ifdef MITA_TRACE
-#define MITA_TRACE_EV(role, tag) ::mita::trace_ev(role, tag)
-#define MITA_TRACE_INIT(id) ::mita::trace_init(id)
-#define MITA_TRACE_FINI() ::mita::trace_fini()
-#else
-#define MITA_TRACE_EV(role, tag) ((void)0)
-#define MITA_TRACE_INIT(id) ((void)0)
-#define MITA_TRACE_FINI() ((void)0)
-#endif
-
 }  // namespace mita

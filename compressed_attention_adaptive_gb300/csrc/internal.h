@@ -22,6 +22,7 @@ void count_launch(int n = 1);
 namespace mita {
 mita_status validate(const mita_params* p);
 mita_status report_error(mita_status st, const char* msg);
+void clear_error();  // empties the calling thread's mita_last_error() detail
 mita_status forward_on_workspace(const mita_params* p, const void* Q, const void* K, const void* V, void* O,
                                  void* ws, size_t ws_bytes, void* stream);
 

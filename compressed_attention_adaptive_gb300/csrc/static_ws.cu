@@ -29,6 +29,7 @@ void* g_static_addr[kMaxDevices] = {};  // device address of g_static_ws per dev
 extern "C" mita_status mita_forward_static(const mita_params* p, const void* Q, const void* K, const void* V,
                                            void* O, int32_t* status_out, void* stream) {
     using namespace mita;
+    clear_error();
     mita_status st = validate(p);
     if (st) return st;
     const size_t need = mita_workspace_size(p);

@@ -23,28 +23,6 @@
 namespace mita {
 using namespace tc;
 
-#ifdef MITA_TRACE
-// Each event is (SM clock << 8 | tag) in a per-role log of block 0.
-constexpr int kTraceCap = 16384;
-__device__ unsigned long long g_mita_trace[4 * kTraceCap];
-__device__ int g_mita_trace_n[4];
-__device__ int g_mita_trace_sel = 1;  // id of the kernel that records
-__shared__ int s_mita_trace_n[4];  // one recording thread per role: plain increments
-__shared__ int s_mita_trace_on;
-__device__ __forceinline__ void trace_init(int id) {
-    if (threadIdx.x < 4) s_mita_trace_n[threadIdx.x] = 0;
-    if (threadIdx.x == 0) s_mita_trace_on = g_mita_trace_sel == id;
-}
-__device__ __forceinline__ void trace_fini() {
-    if (s_mita_trace_on && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 4)
-        g_mita_trace_n[threadIdx.x] = s_mita_trace_n[threadIdx.x];
-}
-__device__ __forceinline__ void trace_ev(int role, int tag) {
-    if (!s_mita_trace_on || blockIdx.x != 0 || blockIdx.y != 0) return;
-    const int i = s_mita_trace_n[role]++;
-    if (i >= 0 && i < kTraceCap) g_mita_trace[role * kTraceCap + i] = ((unsigned long long)clock64() << 8) | (unsigned)tag;
-}
-#endif
 
 namespace {
 
@@ -367,7 +345,6 @@ __global__ void __launch_bounds__(320, 1)
         abort_flag = 0;
         fence_mbar_init();
     }
-    MITA_TRACE_INIT(3);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -389,7 +366,6 @@ __global__ void __launch_bounds__(320, 1)
             for (int c = 0; c < nc; ++c) {
                 const int st = c % NS, use = c / NS;
                 if (!ws_wait(&kv_empty[st], (use & 1) ^ 1, status, abort_v)) break;
-                MITA_TRACE_EV(0, 3);
                 mbar_expect_tx(&kv_full[st], 2 * TILE);
                 const int y = bh * N + j_begin + c * kT;  // rows past the split are masked, past the end read 0
 #pragma unroll
@@ -408,7 +384,6 @@ __global__ void __launch_bounds__(320, 1)
             fence_proxy_async();  // the landmark tiles came through cp.async (generic proxy)
             auto flush_pv = [&](int h) -> bool {
                 if (!ws_wait(&p_full[h & 1], (h >> 1) & 1, status, abort_v)) return false;
-                MITA_TRACE_EV(1, 14);
                 fence_after_sync();
                 issue_pv_ts<D>(tmem + kO, tmem + kS0 + (h & 1) * 128, smem_u32(sV + (h % NS) * TILE), h > 0);
                 mma_commit(&pv_done);
@@ -419,12 +394,10 @@ __global__ void __launch_bounds__(320, 1)
             for (int c = 0; c < nc && ok; ++c) {
                 const int st = c % NS, sb = c & 1;
                 if (!(ok = ws_wait(&kv_full[st], (c / NS) & 1, status, abort_v))) break;
-                MITA_TRACE_EV(1, 11);
                 fence_after_sync();
                 issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sHi), smem_u32(sK + st * TILE), false);
                 issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sLo), smem_u32(sK + st * TILE), true);
                 mma_commit(&s_full[sb]);
-                MITA_TRACE_EV(1, 13);
                 if (c > 0 && !(ok = flush_pv(c - 1))) break;
             }
             if (ok) flush_pv(nc - 1);
@@ -446,7 +419,6 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < nc; ++c) {
             const int sb = c & 1, j0 = j_begin + c * kT;
             if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (c >> 1) & 1, status, abort_v))) { ok = false; break; }
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 21);
             fence_after_sync();
             const uint32_t tS = lane_base(tmem) + kS0 + sb * 128;
             const int nval = row_ok ? min(kT, j_end - j0) - 64 * wg : 0;
@@ -467,7 +439,6 @@ __global__ void __launch_bounds__(320, 1)
                 }
             }
             xmax[c & 1][wg][r] = mx;
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 23);
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&xbar[c & 1]);
@@ -511,7 +482,6 @@ __global__ void __launch_bounds__(320, 1)
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[c & 1]);
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 22);
         }
         if (ok && __all_sync(0xffffffffu, ws_wait(&o_full, 0, status, abort_v))) {
             fence_after_sync();
@@ -537,7 +507,6 @@ __global__ void __launch_bounds__(320, 1)
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    MITA_TRACE_FINI();
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
@@ -777,7 +746,6 @@ __global__ void __launch_bounds__(320, 1)
         abort_flag = 0;
         fence_mbar_init();
     }
-    MITA_TRACE_INIT(2);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -796,7 +764,6 @@ __global__ void __launch_bounds__(320, 1)
             const int st = tl % NSQ;
             int okw = 1;
             if (lane == 0) okw = ws_wait(&q_empty[st], ((tl / NSQ) & 1) ^ 1, status, abort_v);
-            if (lane == 0) MITA_TRACE_EV(0, 1);
             if (!__shfl_sync(0xffffffffu, okw, 0)) break;
             if (lane == 0) {
                 qgen[st] = gen + (reload ? 1 : 0);
@@ -837,19 +804,16 @@ __global__ void __launch_bounds__(320, 1)
             auto flush = [&]() -> bool {
                 const int ob = ptl & 1;
                 if (!ws_wait(&p_full[ptl & 1], (ptl >> 1) & 1, status, abort_v)) return false;
-                MITA_TRACE_EV(1, 14);
                 if (!ws_wait(&o_free[ob], ((ptl >> 1) & 1) ^ 1, status, abort_v)) return false;
                 fence_after_sync();
                 issue_pv_ts<D>(tmem + kO0 + ob * D, tmem + kR0 + (ptl & 1) * 128, smem_u32(sVt), false);
                 mma_commit(&o_full[ob]);
-                MITA_TRACE_EV(1, 15);
                 pending = false;
                 return true;
             };
             for (int tl = 0; tl < nloc; ++tl) {
                 const int st = tl % NSQ, rb = tl & 1;
                 if (!(ok = ws_wait(&q_full[st], (tl / NSQ) & 1, status, abort_v))) break;
-                MITA_TRACE_EV(1, 10);
                 const int gen = qgen[st];
                 if (gen != cur_gen) {
                     // new landmarks: the previous tile's P Vt first, then release the old
@@ -865,7 +829,6 @@ __global__ void __launch_bounds__(320, 1)
                 issue_qk<D>(tmem + kR0 + rb * 128, smem_u32(sQ + st * TILE), smem_u32(sLo), true);
                 mma_commit(&r_full[rb]);
                 mma_commit(&q_empty[st]);
-                MITA_TRACE_EV(1, 13);
                 if (pending && !(ok = flush())) break;
                 pending = true;
                 ptl = tl;
@@ -886,7 +849,6 @@ __global__ void __launch_bounds__(320, 1)
             const int ob = pt & 1;
             const int bh = head(pt), q0 = ((t_begin + pt) % tiles_per_head) * kT, q = q0 + r;
             if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (pt >> 1) & 1, status, abort_v))) return false;
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 25);
             fence_after_sync();
             float o[DH];
 #pragma unroll
@@ -927,7 +889,6 @@ __global__ void __launch_bounds__(320, 1)
                 __syncwarp();
             }
             if (wg == 0 && q < N) sh_lse[(size_t)bh * N + q] = mx + __log2f(lt);
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 27);
             return true;
         };
         bool ok = true;
@@ -937,7 +898,6 @@ __global__ void __launch_bounds__(320, 1)
             const int bh = head(tl), q = ((t_begin + tl) % tiles_per_head) * kT + r;
             const bool q_ok = q < N;
             if (!__all_sync(0xffffffffu, ws_wait(&r_full[rb], (tl >> 1) & 1, status, abort_v))) { ok = false; break; }
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 21);
             fence_after_sync();
             const uint32_t tR = lane_base(tmem) + kR0 + rb * 128;
             const int nval = min(64, m - 64 * wg);  // landmarks of this half
@@ -977,7 +937,6 @@ __global__ void __launch_bounds__(320, 1)
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[rb]);
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 22);
             // routes: this half's s best (v is consumed), the second half's list
             // handed to the first, which merges it after its own (higher indices)
             uint32_t bu[SMAX];
@@ -1003,7 +962,6 @@ __global__ void __launch_bounds__(320, 1)
                         if (u < s) Erow[u] = bi[u];
                 }
             }
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 23);
             // the other half posted its share before this tile's exchange
             if (tl > 0 && !(ok = epilogue(tl - 1, plsum, pmx, plsum + xl[(tl - 1) & 1][wg ^ 1][r]))) break;
             plsum = lsum;
@@ -1014,7 +972,6 @@ __global__ void __launch_bounds__(320, 1)
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    MITA_TRACE_FINI();
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
@@ -1373,7 +1330,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         abort_flag = 0;
         fence_mbar_init();
     }
-    MITA_TRACE_INIT(1);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -1391,7 +1347,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             const int qs = tseq & 1;
             int ok = 1;
             if (lane == 0) ok = ws_wait(&q_empty[qs], ((tseq >> 1) & 1) ^ 1, status, abort_v);
-            if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 1);
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             const int4 td = tiles[t_begin + tseq];
             const int bh = td.x, e = td.y, start = td.z, rows = td.w & 255, shrows = td.w >> 8;
@@ -1420,7 +1375,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&q_full[qs]);  // publishes this warp's rowq rows (and tinfo)
             }
-            if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 2);
             // key rows of chunk c into keyrow[buf]: landmark rows for the shared
             // chunks, I_e entries for the expert's chunks
             auto load_keys = [&](int c, int buf) {
@@ -1448,7 +1402,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 const int st = g & 1;
                 int okw = 1;
                 if (lane == 0) okw = ws_wait(&kv_empty[st], ((g >> 1) & 1) ^ 1, status, abort_v);
-                if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 3);
                 if (!__shfl_sync(0xffffffffu, okw, 0)) { ok2 = false; break; }
                 __syncwarp();
                 {
@@ -1467,10 +1420,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     }
                     cp_async_arrive(&kv_full[st]);
                 }
-                if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 4);
                 // the next chunk's key rows load while this stage fills and the next one drains
                 if (c + 1 < nch) load_keys(c + 1, (g + 1) & 1);
-                if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 5);
                 __syncwarp();
             }
             if (!ok2) break;
@@ -1488,7 +1439,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             int pg = 0;
             auto flush_pv = [&]() -> bool {
                 if (!ws_wait(&p_full[pg & 1], (pg >> 1) & 1, status, abort_v)) return false;
-                MITA_TRACE_EV(1, 14);
                 if (pm.first && !ws_wait(&o_free[pm.ob], ((pm.tseq >> 1) & 1) ^ 1, status, abort_v)) return false;
                 fence_after_sync();
                 issue_pv<D>(tmem + kO0 + pm.ob * 128, smem_u32(sK + pm.st * KP), smem_u32(sV + pm.st * TILE),
@@ -1496,28 +1446,23 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 mma_commit(&pv_done);
                 mma_commit(&kv_empty[pm.st]);
                 if (pm.last) mma_commit(&o_full[pm.ob]);
-                MITA_TRACE_EV(1, 15);
                 pending = false;
                 return true;
             };
             for (; tseq < nloc;) {
                 const int qs = tseq & 1;
                 if (!(ok = ws_wait(&q_full[qs], (tseq >> 1) & 1, status, abort_v))) break;
-                MITA_TRACE_EV(1, 10);
                 const WsTile ti = tinfo[qs];
                 if (ti.rows < 0) break;
                 for (int c = 0; c < ti.nch; ++c, ++g) {
                     const int st = g & 1, sb = g & 1;
                     if (!(ok = ws_wait(&kv_full[st], (g >> 1) & 1, status, abort_v))) break;
-                    MITA_TRACE_EV(1, 11);
                     if (!(ok = ws_wait(&s_free[sb], ((g >> 1) & 1) ^ 1, status, abort_v))) break;
-                    MITA_TRACE_EV(1, 12);
                     fence_proxy_async();  // copied tiles (generic proxy) -> the MMA's async-proxy reads
                     fence_after_sync();
                     issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sQ + qs * TILE), smem_u32(sK + st * KP), false);
                     mma_commit(&s_full[sb]);
                     const bool last = c == ti.nch - 1;
-                    MITA_TRACE_EV(1, 13);
                     if (last) mma_commit(&q_empty[qs]);
                     if (pending && !(ok = flush_pv())) break;
                     pending = true;
@@ -1537,7 +1482,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         for (; tseq < nloc;) {
             const int qs = tseq & 1, ob = tseq & 1;
             if (!__all_sync(0xffffffffu, ws_wait(&q_full[qs], (tseq >> 1) & 1, status, abort_v))) break;
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 20);
             const WsTile ti = tinfo[qs];
             if (ti.rows < 0) break;
             const int pk = rowq[qs][r];
@@ -1547,7 +1491,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             for (int c = 0; c < ti.nch; ++c, ++g) {
                 const int sb = g & 1;
                 if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (g >> 1) & 1, status, abort_v))) { ok = false; break; }
-                if (threadIdx.x == 0) MITA_TRACE_EV(2, 21);
                 fence_after_sync();
                 const bool shc = c < ti.nsh;
                 const int nk = shc ? min(kT, m - c * kT) : min(kT, k - (c - ti.nsh) * kT);
@@ -1564,7 +1507,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_free[sb]);  // S(g) is read: its buffer may take S(g+2)
-                if (threadIdx.x == 0) MITA_TRACE_EV(2, 22);
                 const int nval = row_ok ? nk : 0;  // columns of this row that hold a valid key
                 float mx = -INFINITY;
 #pragma unroll
@@ -1621,12 +1563,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[g & 1]);
-                if (threadIdx.x == 0) MITA_TRACE_EV(2, 24);
             }
             if (!ok) break;
             // epilogue: normalized partial (or output) of each valid row
             if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (tseq >> 1) & 1, status, abort_v))) break;
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 25);
             fence_after_sync();
             const uint32_t tO = lane_base(tmem) + kO0 + ob * 128;
             const bool valid = q >= 0;
@@ -1653,16 +1593,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                                        pack_bf16(o[c0 + 4] * inv, o[c0 + 5] * inv), pack_bf16(o[c0 + 6] * inv, o[c0 + 7] * inv));
                 }
             }
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 26);
             if (valid && s > 1) merge_partials<D>(O, part, lse, cnt, bh, N, q, s, pr, mref + __log2f(l));
             ++tseq;
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 27);
         }
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    MITA_TRACE_FINI();
     if (warp == 4 + kNPW) tmem_dealloc(tmem, 512);
 }
 
@@ -1744,7 +1681,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
         abort_flag = 0;
         fence_mbar_init();
     }
-    MITA_TRACE_INIT(1);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -1766,7 +1702,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
             {
                 int ok = 1;
                 if (lane == 0) ok = ws_wait(&q_empty[qs], ((tl >> 1) & 1) ^ 1, status, abort_v);
-                if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 1);
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             }
             // this warp's rows: (query, slot) from the bucket order, -1 past the tile's rows
@@ -1793,7 +1728,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&q_full[qs]);  // publishes this warp's rowq rows (and tinfo)
             }
-            if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 2);
             if (reload) {
                 const __nv_bfloat16* Kb = K + (size_t)bh * N * D;
                 const __nv_bfloat16* Vb = V + (size_t)bh * N * D;
@@ -1827,7 +1761,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
                         cp_async16(dv + sw_off(r, cc, kT), Vb + off, true);
                     }
                     cp_async_arrive(&kv_full[c]);
-                    if (pw == 0 && lane == 0) MITA_TRACE_EV(0, 4);
                     __syncwarp();
                 }
                 if (!okc) break;
@@ -1851,7 +1784,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
                     const int tl = ns / nex, c = ns - tl * nex, qs = tl & 1;
                     if (tl != seen_tl) {
                         if (!(ok = ws_wait(&q_full[qs], (tl >> 1) & 1, status, abort_v))) break;
-                        MITA_TRACE_EV(1, 10);
                         s_gen = tinfo[qs].gen;
                         seen_tl = tl;
                     }
@@ -1866,20 +1798,17 @@ __global__ void __launch_bounds__(kResThreads, 1)
                         cur_gen = s_gen;
                     }
                     if (!(ok = ws_wait(&kv_full[c], (s_gen - 1) & 1, status, abort_v))) break;
-                    MITA_TRACE_EV(1, 11);
                     fence_proxy_async();  // copied tiles (generic proxy) -> the MMA's async-proxy reads
                     fence_after_sync();
                     issue_qk<D>(tmem + kS0 + (ns & 1) * 128, smem_u32(sQ + qs * TILE), smem_u32(sK + c * TILE), false);
                     mma_commit(&s_full[ns & 1]);
                     if (c == nex - 1) mma_commit(&q_empty[qs]);
-                    MITA_TRACE_EV(1, 13);
                     ++ns;
                 }
                 if (!ok) break;
                 // O += P V of chunk g
                 const int tl = g / nex, c = g - tl * nex, ob = tl & 1;
                 if (!(ok = ws_wait(&p_full[g & 1], (g >> 1) & 1, status, abort_v))) break;
-                MITA_TRACE_EV(1, 14);
                 if (c == 0 && !(ok = ws_wait(&o_free[ob], ((tl >> 1) & 1) ^ 1, status, abort_v))) break;
                 fence_after_sync();
                 issue_pv_ts<D>(tmem + kO0 + ob * 128, tmem + kS0 + (g & 1) * 128, smem_u32(sV + c * TILE), c > 0);
@@ -1889,7 +1818,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
                     mma_commit(&kv_rel[nex - 1]);
                     rel_last = false;
                 }
-                MITA_TRACE_EV(1, 15);
             }
         }
         __syncwarp();
@@ -1910,7 +1838,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
             constexpr int PPR = DH / 8, RPI = 32 / PPR;  // pieces per half row, rows per store instruction
             const int ob = pt & 1;
             if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (pt >> 1) & 1, status, abort_v))) return false;
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 25);
             fence_after_sync();
             const uint32_t tO = lane_base(tmem) + kO0 + ob * 128 + wg * DH;
             float o[DH];
@@ -1955,7 +1882,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 __syncwarp();
             }
             if (wg == 0 && pk >= 0) lse[pr] = pm + __log2f(lt);
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 27);
             return true;
         };
         int g = 0;
@@ -1966,7 +1892,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
         for (int tl = 0; tl < nloc && ok; ++tl) {
             const int qs = tl & 1, ob = tl & 1;
             if (!__all_sync(0xffffffffu, ws_wait(&q_full[qs], (tl >> 1) & 1, status, abort_v))) break;
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 20);
             const ResTile ti = tinfo[qs];
             const int pk = rowq[qs][r];
             __syncwarp();
@@ -1977,7 +1902,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
             for (int c = 0; c < nex; ++c, ++g) {
                 const int sb = g & 1;
                 if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (g >> 1) & 1, status, abort_v))) { ok = false; break; }
-                if (threadIdx.x == 0) MITA_TRACE_EV(2, 21);
                 fence_after_sync();
                 const uint32_t tS = lane_base(tmem) + kS0 + sb * 128;
                 const int nval = valid ? min(kT, k - c * kT) - 64 * wg : 0;  // valid columns of this half
@@ -2030,7 +1954,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 // P (bf16, two keys per column) over the scores: keys 64wg.. -> columns 32wg..
                 tmem_st32(tS + 32 * wg, reinterpret_cast<const float*>(pkd));
                 tmem_wait_st();
-                if (threadIdx.x == 0) MITA_TRACE_EV(2, 22);
                 l = l * alpha + sum;
                 mref = mnew;
                 if (__any_sync(0xffffffffu, c > 0 && alpha != 1.0f)) {
@@ -2060,7 +1983,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
                     have_prev = false;
                 }
             }
-            if (threadIdx.x == 0) MITA_TRACE_EV(2, 24);
             if (!ok) break;
             have_prev = true;
             pti = ti;
@@ -2073,7 +1995,6 @@ __global__ void __launch_bounds__(kResThreads, 1)
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    MITA_TRACE_FINI();
     if (warp == 8 + kNPW) tmem_dealloc(tmem, 512);
 }
 
@@ -2316,18 +2237,3 @@ cudaError_t launch_forward_tc(const Dims& D, const TcPlan& P, const TcWork& W, c
 
 }  // namespace mita
 
-#ifdef MITA_TRACE
-// Trace builds only: copies the event logs out and clears them.
-extern "C" int mita_trace_read(unsigned long long* host, int* counts) {
-    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-    cudaMemcpyFromSymbol(host, mita::g_mita_trace, sizeof(unsigned long long) * 4 * mita::kTraceCap);
-    cudaMemcpyFromSymbol(counts, mita::g_mita_trace_n, sizeof(int) * 4);
-    int zero[4] = {0, 0, 0, 0};
-    cudaMemcpyToSymbol(mita::g_mita_trace_n, zero, sizeof zero);
-    return 0;
-}
-// Trace builds only: which kernel records (1 expert attention, 2 routing).
-extern "C" int mita_trace_select(int id) {
-    return cudaMemcpyToSymbol(mita::g_mita_trace_sel, &id, sizeof id) == cudaSuccess ? 0 : -1;
-}
-#endif

@@ -39,7 +39,7 @@ class Workload:
     k: int
     s: int
     dtype: str               # "f32" | "bf16"
-    kind: str                # "iid" | "grf2d" | "clustered"
+    kind: str                # "iid" | "grf2d" | "clustered" | "ties"
     grid: tuple = None       # (grid_h, grid_w) for 2-D pooling
     lm: tuple = None         # (lm_h, lm_w) landmark grid for 2-D pooling
     k_centers: int = 64      # clustered: number of key centers
@@ -48,6 +48,7 @@ class Workload:
     q_noise: float = 0.5     # clustered: Q = K + q_noise * N(0, 1)
     length_scale: float = 8.0  # grf2d
     noise: float = 0.1       # grf2d: additive white-noise std
+    zero_frac: float = 0.0   # ties: fraction of key rows set to zero (half of them -0.0)
 
     @property
     def BH(self):
@@ -169,6 +170,31 @@ def _head(w: Workload, seed: int, b: int, h: int):
             V = cv[z] + np.float32(w.spread) * rv.standard_normal((N, d), dtype=np.float32)
         rq = _rng(seed, w, b, h, "Q")
         Q = K + np.float32(w.q_noise) * rq.standard_normal((N, d), dtype=np.float32)
+        return Q, K, V
+    if w.kind == "ties":
+        # Small integers drawn from k_centers row patterns, so that raw scores
+        # are exact in float32 and float64 and many of them are exactly equal.
+        # Keys: pattern rows plus a zero_frac share of zero rows, half of them
+        # -0.0. Queries: the first half of the 1-D pooling windows repeat a
+        # period dividing the window, so their landmarks are identical (exact
+        # routing ties); the rest are random pattern rows. With power-of-two
+        # windows every landmark (a window mean) is exact too.
+        rk = _rng(seed, w, b, h, "K")
+        pat = rk.integers(-2, 3, size=(w.k_centers, d)).astype(np.float32)
+        K = pat[rk.integers(0, w.k_centers, size=N)]
+        nz = int(round(w.zero_frac * N))
+        if nz:
+            zr = rk.choice(N, nz, replace=False)
+            K[zr] = 0.0
+            K[zr[::2]] = -0.0
+        rq = _rng(seed, w, b, h, "Q")
+        qpat = rq.integers(-2, 3, size=(w.k_centers, d)).astype(np.float32)
+        Q = qpat[rq.integers(0, w.k_centers, size=N)]
+        win = N // w.m
+        period = 4 if win % 4 == 0 and w.k_centers >= 4 else 1
+        half = (w.m // 2) * win
+        Q[:half] = qpat[np.arange(half) % period]
+        V = _rng(seed, w, b, h, "V").standard_normal((N, d), dtype=np.float32)
         return Q, K, V
     raise ValueError(w.kind)
 

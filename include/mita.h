@@ -35,6 +35,9 @@
  *     A failed launch returns MITA_ERR_CUDA. Errors detected on the device
  *     (an index out of range, a bounded wait that ran out) are written to a
  *     status word inside the workspace and read with mita_device_status().
+ *     The first kernel of every call resets that word, so it holds the first
+ *     device-side error of the most recent call on the workspace: read it
+ *     after each call whose device status matters.
  *   - Calls are reentrant; concurrent calls must use distinct workspaces.
  */
 #ifndef MITA_H
@@ -120,7 +123,8 @@ mita_status mita_forward_host(const mita_params* p, const void* Q, const void* K
                               void* dev, size_t dev_bytes, void* stream);
 
 /* Synchronizes `stream`, returns the device status word of workspace `ws`
- * (MITA_OK if no device-side error was recorded) and clears it. */
+ * (MITA_OK if no device-side error was recorded by the most recent call on
+ * `ws`) and clears it. */
 mita_status mita_device_status(void* ws, void* stream);
 
 /* Static description of a status code. */

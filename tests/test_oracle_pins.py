@@ -75,6 +75,35 @@ def test_hand_example():
     np.testing.assert_allclose(r["O"].ravel(), g["O"], rtol=1e-14)
 
 
+# ------------------------------------------------------------ raw scores
+# oracle.scores supplies every raw score the parity rules judge (top-k sets on
+# k_j . qt_i, routes on q . qt_i), so it is pinned on its own.
+
+@pytest.mark.parametrize("na,nb,d", [(7, 13, 5), (1, 40, 128), (33, 2, 64)])
+def test_scores_match_numpy_matmul(na, nb, d):
+    A, B = _rand((na, d), 11), _rand((nb, d), 12)
+    got = oracle.scores(A, B)
+    assert got.shape == (na, nb)
+    np.testing.assert_allclose(got, A @ B.T, rtol=1e-12, atol=1e-12)
+
+
+def test_scores_exact_on_integers():
+    # small-integer inputs: every product and sum is exact in float64, so the
+    # scores must equal the int64 matrix product exactly
+    rng = np.random.default_rng(13)
+    A = rng.integers(-50, 51, size=(9, 31))
+    B = rng.integers(-50, 51, size=(17, 31))
+    np.testing.assert_array_equal(oracle.scores(A.astype(np.float64), B.astype(np.float64)), (A @ B.T).astype(np.float64))
+
+
+def test_scores_orientation():
+    # A = unit rows e_c picks coordinate c of every row of B: S = B^T
+    d, nb = 6, 10
+    B = _rand((nb, d), 14)
+    np.testing.assert_array_equal(oracle.scores(np.eye(d), B), B.T)
+    np.testing.assert_array_equal(oracle.scores(B, np.eye(d)), B)
+
+
 # ------------------------------------------------------ top-k and routing
 
 def _brute_topk(S, k):
