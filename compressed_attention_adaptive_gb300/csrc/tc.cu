@@ -127,14 +127,16 @@ __device__ __forceinline__ void load_tile(uint32_t sbase, RowPtr src_row) {
     load_rows<D>(sbase, kT, src_row);
 }
 
-// Keeps the SMAX largest keys seen so far, descending; a key equal to one
-// already held stays behind it, so with increasing indices ties go to the
-// lower index.
+// Keeps the SMAX largest keys seen so far, ordered by key descending and, for
+// equal keys, index ascending (ties to the lower index). The comparison holds
+// for the entry being inserted and for every entry it displaces down the list
+// (a displaced entry can have a lower index than an equal key behind it).
+// Empty slots are key 0, index -1 (every real key is > 0).
 template <int SMAX>
 __device__ __forceinline__ void top_insert(uint32_t (&bu)[SMAX], int (&bi)[SMAX], uint32_t u, int i) {
 #pragma unroll
     for (int t = 0; t < SMAX; ++t) {
-        const bool gt = u > bu[t];
+        const bool gt = u > bu[t] || (u == bu[t] && (uint32_t)i < (uint32_t)bi[t]);
         const uint32_t tu = bu[t];
         const int ti = bi[t];
         bu[t] = gt ? u : tu;
