@@ -2,8 +2,8 @@
 """Throughput of the MiTA attention forward pass on GB300, one JSON line.
 
 A step is one full forward pass (landmark pooling, landmark pass with the
-shared expert, top-k expert sets, routing, bucketing, expert attention with
-the merge) over one batch of synthetic inputs already resident in HBM, through
+shared expert, top-k expert sets, routing, bucketing, expert attention fused
+with the merge) over one batch of synthetic inputs already resident in HBM, through
 the C ABI ``mita_forward``. The default workload is the 32k-token long-context
 case (B=2, H=16, N=32768, d=128, m=128, k=256, s=2, bf16). Inputs (805 MB)
 are larger than L2, so no flush is needed between steps.
@@ -256,9 +256,10 @@ def expert_roofline(w, phase_ms, pk, pk_src, ms_step):
     launching stream around the launch, inside the timed region), against the
     measured burst bf16 peak (the step is milliseconds long, not a sustained
     seconds-long loop); the sustained peak is given beside it."""
-    resident = "merge" in phase_ms  # k_expert_res; the shared slots ran in the routing pass
+    phase = next(k for k in phase_ms if k.startswith("expert"))
+    resident = phase == "expert_res"  # k_expert_res; the shared slots ran in the routing pass
     flops = expert_flops(w, with_shared=not resident)
-    ms = phase_ms["expert"]
+    ms = phase_ms[phase]
     achieved = flops / (ms * 1e-3) / 1e12
     kernel = "k_expert_res" if resident else "k_expert_ws"
     traffic = None
@@ -360,7 +361,8 @@ def main():
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "m": w.m, "k": w.k, "s": w.s,
                        "path": "tcgen05" if uses_tc else "cuda-core", "l2": "inputs larger than L2 (no flush)",
                        "parallelism": "replicas x%d" % world},
-            "roofline": expert_roofline(w, phase_ms, pk, pk_src, ms_step) if "expert" in phase_ms else None,
+            "roofline": expert_roofline(w, phase_ms, pk, pk_src, ms_step)
+            if any(k.startswith("expert") for k in phase_ms) else None,
             "path_roofline": {"t_roof_us": t_roof * 1e6, "frac": t_roof / (ms_step * 1e-3),
                               "flops": F, "compulsory_bytes": Bytes,
                               "peaks": {"bf16_tflops": pk["bf16_tflops"], "hbm_gbs": pk["hbm_gbs"],

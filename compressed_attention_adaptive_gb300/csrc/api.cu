@@ -67,7 +67,8 @@ static mita_status resolve(const mita_params* p, Dims* D) {
     if (p->s < 1 || p->s > p->m) return fail(MITA_ERR_INVALID_ARG, "s must be in [1, m]");
     if (p->s > kMaxS) return fail(MITA_ERR_UNSUPPORTED, "s > %d is not supported", kMaxS);
     if (p->dtype != MITA_DTYPE_F32 && p->dtype != MITA_DTYPE_BF16) return fail(MITA_ERR_INVALID_ARG, "bad dtype");
-    if (p->flags & ~(unsigned)(MITA_FLAG_NO_SHARED | MITA_FLAG_SIMT)) return fail(MITA_ERR_INVALID_ARG, "unknown flag");
+    if (p->flags & ~(unsigned)(MITA_FLAG_NO_SHARED | MITA_FLAG_SIMT | MITA_TESTFLAG_STALL_PRODUCER))
+        return fail(MITA_ERR_INVALID_ARG, "unknown flag");
     if (!(p->scale >= 0.0f) || isinf(p->scale)) return fail(MITA_ERR_INVALID_ARG, "scale must be finite and >= 0");
     if ((long long)p->B * p->H > 65535) return fail(MITA_ERR_UNSUPPORTED, "B*H must be <= 65535");
     if ((long long)p->B * p->H * p->N >= (1LL << 31)) return fail(MITA_ERR_UNSUPPORTED, "B*H*N must be < 2^31");
@@ -158,6 +159,7 @@ static Work carve(const Dims& D, void* ws, size_t* bytes) {
         t.cursors = c.take<int>(BH * D.m * 2);
         t.toff = c.take<int>(BH * D.m);
         t.tiles = c.take<int4>((size_t)P.max_tiles);
+        t.xtl = c.take<int2>(BH * D.m);
         t.perm = c.take<int32_t>(BH * D.N * D.s);
         t.part = c.take<__nv_bfloat16>(BH * D.N * D.s * D.d);
         t.lse = c.take<float>(BH * D.N * D.s);

@@ -13,7 +13,7 @@ enum : int { kStOk = 0, kStTimeout = 5, kStBounds = 6 };
 
 // Internal flag bit in Dims::flags (never a public MITA_FLAG_*): the call is
 // one part of a larger one, so its first kernel keeps the device status word.
-constexpr unsigned kFlagKeepStatus = 1u << 31;
+constexpr unsigned kFlagKeepStatus = 1u << 30;
 
 // Problem dimensions after validation (1-D pooling is a 1 x N grid).
 struct Dims {

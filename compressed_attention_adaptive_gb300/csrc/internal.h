@@ -73,12 +73,13 @@ struct TcWork {
     int2* cand;                      // [BH][m_pad][splits][2][cand_cap / 2] (score, key) records
     int* ccount;                     // [BH][m_pad][splits][2]
     int* counts;                     // [BH][m][2]
-    int* tile_ctr;                   // [2]: tiles written, tiles taken
+    int* tile_ctr;                   // [2]: tiles written, experts claimed by the expert attention
     void* zero_begin;                // counts .. tile_ctr, cleared each call
     size_t zero_bytes;
     int* cursors;                    // [BH][m][2]
     int* toff;                       // [BH][m]
     int4* tiles;                     // [max_tiles]
+    int2* xtl;                       // [BH][m] (first tile, tile count) of each expert
     int32_t* perm;                   // [BH][N*s]
     __nv_bfloat16* part;             // [BH][N][s][d]
     float* lse;                      // [BH][N][s]

@@ -158,7 +158,7 @@ struct CandSrc {
             for (int t = threadIdx.x; t < n; t += blockDim.x) f(skey[t], sidx[t]);
         } else {
             for (int sp = 0; sp < splits; ++sp) {
-                const int c = counts[sp];
+                const int c = (int)min((long long)max(counts[sp], 0), cap);
                 const int2* b = base + sp * cap;
                 for (int t = threadIdx.x; t < c; t += blockDim.x) {
                     const int2 r = b[t];
@@ -235,12 +235,15 @@ __global__ void __launch_bounds__(512) k_topk_cand(const int2* __restrict__ cand
     for (int w = threadIdx.x; w < nwords; w += blockDim.x) bits[w] = 0u;
     // region counts: read in parallel (up to kMaxRegions staged), then prefix offsets
     __shared__ int sh_cnt[kMaxRegions];
-    for (int sp = threadIdx.x; sp < kMaxRegions; sp += blockDim.x) sh_cnt[sp] = sp < splits ? cnts[sp] : 0;
+    // a region never holds more than cap records; the clamp keeps every read in
+    // bounds even when a landmark pass gave up before writing its counts
+    auto region_count = [&](int sp) { return (int)min((long long)max(cnts[sp], 0), cap); };
+    for (int sp = threadIdx.x; sp < kMaxRegions; sp += blockDim.x) sh_cnt[sp] = sp < splits ? region_count(sp) : 0;
     __syncthreads();
     if (threadIdx.x == 0) {
         int tot = 0;
         for (int sp = 0; sp < splits; ++sp) {
-            const int c = sp < kMaxRegions ? sh_cnt[sp] : cnts[sp];
+            const int c = sp < kMaxRegions ? sh_cnt[sp] : region_count(sp);
             if (sp < kMaxRegions) sh_off[sp] = tot;
             tot += c;
         }

@@ -57,21 +57,40 @@ __device__ __forceinline__ bool sync_on_mma(uint64_t* bar, uint32_t& phase, int*
     return !bad;
 }
 
+// Wait budgets in SM clock cycles: about one second normally; about one
+// millisecond for a launch that injects a stall (the fault tests).
+constexpr long long kSpin = 2LL << 30, kSpinTest = 1LL << 21;
+
 // Bounded wait used by the warp-specialized kernels: gives up when another
-// role has set the abort flag, or after about a second (then sets the device
+// role has set the abort flag, or after `lim` cycles (then sets the device
 // status and the abort flag itself).
-__device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort_flag) {
+__device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort_flag,
+                                        long long lim = kSpin) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
         if (*abort_flag) return false;
-        if (clock64() - t0 > (2LL << 30)) {
+        if (clock64() - t0 > lim) {
             set_status(status, kStTimeout);
             *abort_flag = 1;
             return false;
         }
     }
     return true;
+}
+
+// Waits (bounded, ignoring the abort flag) for work this CTA has already
+// issued to the asynchronous units (MMAs, TMA loads) to land, so that the
+// CTA never frees TMEM or exits under them, also after an abort.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* status) {
+    (void)mbar_wait(bar, parity, status);
+}
+
+// Named barrier over `nthreads` threads (a multiple of 32) of the CTA; the
+// calling warp reconverges first.
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    __syncwarp();
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Issues S = A * B^T over the head dim D (K-major A and B tiles of 128 rows).
@@ -308,7 +327,7 @@ __global__ void __launch_bounds__(320, 1)
                   const __nv_bfloat16* __restrict__ Qhi, const __nv_bfloat16* __restrict__ Qlo,
                   const float* __restrict__ thr, int2* __restrict__ cand, int* __restrict__ ccount,
                   float* __restrict__ Opart, float2* __restrict__ ML, int N, int m, int m_pad, int splits,
-                  int chunks_per_split, float sl, int* __restrict__ status) {
+                  int chunks_per_split, float sl, int stall, int* __restrict__ status) {
     constexpr int TILE = kT * D * 2;
     constexpr int DH = D / 2;
     constexpr uint32_t kS0 = 0, kO = 256;
@@ -319,11 +338,12 @@ __global__ void __launch_bounds__(320, 1)
     uint8_t* sK = sm + 2 * TILE;   // NS stages
     uint8_t* sV = sK + NS * TILE;  // NS stages
     __shared__ uint64_t kv_full[NS], kv_empty[NS], s_full[2], p_full[2], xbar[2];
-    __shared__ uint64_t pv_done, o_full, q_bar, ebar;
+    __shared__ uint64_t pv_done, o_full, q_bar, ebar, drain;
     __shared__ float xmax[2][2][kT], xl[2][kT];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     volatile int* abort_v = &abort_flag;
+    const long long lim = stall ? kSpinTest : kSpin;
     const int mt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j_begin = sp * chunks_per_split * kT;
@@ -344,6 +364,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_init(&o_full, 1);
         mbar_init(&q_bar, 32);
         mbar_init(&ebar, 8);
+        mbar_init(&drain, 1);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -365,9 +386,15 @@ __global__ void __launch_bounds__(320, 1)
             cp_async_arrive(&q_bar);
         }
         if (lane == 0) {
+            // fault test: the first CTA never loads its first chunk, so the MMA
+            // warp's bounded wait for it runs out
+            const int skip = (stall && mt == 0 && sp == 0 && bh == 0) ? 0 : -1;
+            int issued = 0;
             for (int c = 0; c < nc; ++c) {
                 const int st = c % NS, use = c / NS;
-                if (!ws_wait(&kv_empty[st], (use & 1) ^ 1, status, abort_v)) break;
+                if (!ws_wait(&kv_empty[st], (use & 1) ^ 1, status, abort_v, lim)) break;
+                issued = c + 1;
+                if (c == skip) continue;
                 mbar_expect_tx(&kv_full[st], 2 * TILE);
                 const int y = bh * N + j_begin + c * kT;  // rows past the split are masked, past the end read 0
 #pragma unroll
@@ -376,16 +403,20 @@ __global__ void __launch_bounds__(320, 1)
                     tma_load_2d(smem_u32(sV + st * TILE) + cb * kT * 128, &tmV, cb * 64, y, &kv_full[st]);
                 }
             }
+            // the loads still in flight (at most the last NS issued) land before
+            // the CTA may exit
+            for (int c = max(0, issued - NS); c < issued; ++c)
+                if (c != skip) drain_wait(&kv_full[c % NS], (c / NS) & 1, status);
         }
         __syncwarp();
         cp_async_wait_all();
     } else if (warp == 9) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            bool ok = ws_wait(&q_bar, 0, status, abort_v);
+            bool ok = ws_wait(&q_bar, 0, status, abort_v, lim);
             fence_proxy_async();  // the landmark tiles came through cp.async (generic proxy)
             auto flush_pv = [&](int h) -> bool {
-                if (!ws_wait(&p_full[h & 1], (h >> 1) & 1, status, abort_v)) return false;
+                if (!ws_wait(&p_full[h & 1], (h >> 1) & 1, status, abort_v, lim)) return false;
                 fence_after_sync();
                 issue_pv_ts<D>(tmem + kO, tmem + kS0 + (h & 1) * 128, smem_u32(sV + (h % NS) * TILE), h > 0);
                 mma_commit(&pv_done);
@@ -395,7 +426,7 @@ __global__ void __launch_bounds__(320, 1)
             };
             for (int c = 0; c < nc && ok; ++c) {
                 const int st = c % NS, sb = c & 1;
-                if (!(ok = ws_wait(&kv_full[st], (c / NS) & 1, status, abort_v))) break;
+                if (!(ok = ws_wait(&kv_full[st], (c / NS) & 1, status, abort_v, lim))) break;
                 fence_after_sync();
                 issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sHi), smem_u32(sK + st * TILE), false);
                 issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sLo), smem_u32(sK + st * TILE), true);
@@ -403,6 +434,9 @@ __global__ void __launch_bounds__(320, 1)
                 if (c > 0 && !(ok = flush_pv(c - 1))) break;
             }
             if (ok) flush_pv(nc - 1);
+            // every MMA this thread issued has completed before TMEM is freed
+            mma_commit(&drain);
+            drain_wait(&drain, 0, status);
         }
         __syncwarp();
     } else {
@@ -420,7 +454,7 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t tO = lane_base(tmem) + kO + wg * DH;
         for (int c = 0; c < nc; ++c) {
             const int sb = c & 1, j0 = j_begin + c * kT;
-            if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (c >> 1) & 1, status, abort_v))) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (c >> 1) & 1, status, abort_v, lim))) { ok = false; break; }
             fence_after_sync();
             const uint32_t tS = lane_base(tmem) + kS0 + sb * 128;
             const int nval = row_ok ? min(kT, j_end - j0) - 64 * wg : 0;
@@ -444,7 +478,7 @@ __global__ void __launch_bounds__(320, 1)
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&xbar[c & 1]);
-            if (!__all_sync(0xffffffffu, ws_wait(&xbar[c & 1], (c >> 1) & 1, status, abort_v))) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, ws_wait(&xbar[c & 1], (c >> 1) & 1, status, abort_v, lim))) { ok = false; break; }
             fence_after_sync();
             mx = fmaxf(mx, xmax[c & 1][wg ^ 1][r]);
             float mnew = mref, alpha = 1.0f;
@@ -467,7 +501,7 @@ __global__ void __launch_bounds__(320, 1)
             mref = mnew;
             if (__any_sync(0xffffffffu, c > 0 && alpha != 1.0f)) {
                 // S(c) done implies PV(c-2) done: this wait can only see PV(c-1)'s phase
-                if (!__all_sync(0xffffffffu, ws_wait(&pv_done, (c - 1) & 1, status, abort_v))) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, ws_wait(&pv_done, (c - 1) & 1, status, abort_v, lim))) { ok = false; break; }
                 fence_after_sync();
                 const float a = (c > 0) ? alpha : 1.0f;
 #pragma unroll 1
@@ -485,7 +519,7 @@ __global__ void __launch_bounds__(320, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[c & 1]);
         }
-        if (ok && __all_sync(0xffffffffu, ws_wait(&o_full, 0, status, abort_v))) {
+        if (ok && __all_sync(0xffffffffu, ws_wait(&o_full, 0, status, abort_v, lim))) {
             fence_after_sync();
             float o[DH];
 #pragma unroll
@@ -495,7 +529,7 @@ __global__ void __launch_bounds__(320, 1)
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ebar);
-            if (__all_sync(0xffffffffu, ws_wait(&ebar, 0, status, abort_v))) {
+            if (__all_sync(0xffffffffu, ws_wait(&ebar, 0, status, abort_v, lim))) {
                 const float lt = l + xl[wg ^ 1][r];
                 const size_t orow = ((size_t)bh * splits + sp) * m_pad + row;
                 float* od = Opart + orow * D + wg * DH;
@@ -845,8 +879,9 @@ __global__ void __launch_bounds__(320, 1)
         const int wg = warp >> 2, r = threadIdx.x & 127;
         uint8_t* stage = sStage + warp * kStageWarp;
         // lt: the whole row sum when the halves already exchanged it (with the next
-        // tile's row maxima), else < 0 and the epilogue exchanges it (last tile)
-        auto epilogue = [&](int pt, float lsum, float mx, float lt) -> bool {
+        // tile's row maxima); last: the CTA's last tile, whose epilogue
+        // exchanges the row sum itself
+        auto epilogue = [&](int pt, float lsum, float mx, float lt, bool last) -> bool {
             constexpr int PPR = DH / 8, RPI = 32 / PPR;  // pieces per half row, rows per store instruction
             const int ob = pt & 1;
             const int bh = head(pt), q0 = ((t_begin + pt) % tiles_per_head) * kT, q = q0 + r;
@@ -856,14 +891,14 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(lane_base(tmem) + kO0 + ob * D + wg * DH + c0, o + c0);
             tmem_wait_ld();
-            if (lt < 0.0f) xl[pt & 1][wg][r] = lsum;
+            if (last) xl[pt & 1][wg][r] = lsum;
             fence_before_sync();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&o_free[ob]);
-                if (lt < 0.0f) mbar_arrive(&ebar);
+                if (last) mbar_arrive(&ebar);
             }
-            if (lt < 0.0f) {  // ebar's only use
+            if (last) {  // ebar's only use
                 if (!__all_sync(0xffffffffu, ws_wait(&ebar, 0, status, abort_v))) return false;
                 lt = lsum + xl[pt & 1][wg ^ 1][r];
             }
@@ -965,11 +1000,11 @@ __global__ void __launch_bounds__(320, 1)
                 }
             }
             // the other half posted its share before this tile's exchange
-            if (tl > 0 && !(ok = epilogue(tl - 1, plsum, pmx, plsum + xl[(tl - 1) & 1][wg ^ 1][r]))) break;
+            if (tl > 0 && !(ok = epilogue(tl - 1, plsum, pmx, plsum + xl[(tl - 1) & 1][wg ^ 1][r], false))) break;
             plsum = lsum;
             pmx = mx;
         }
-        if (ok && nloc > 0) epilogue(nloc - 1, plsum, pmx, -1.0f);
+        if (ok && nloc > 0) epilogue(nloc - 1, plsum, pmx, 0.0f, true);
     }
     fence_before_sync();
     __syncthreads();
@@ -1041,8 +1076,9 @@ __global__ void __launch_bounds__(128)
 // then the others; each bucket is cut into 128-row work tiles.
 
 // counts[bh][e][cls], cls = 0 for slot 0, 1 for slots >= 1.
+// Also clears the per-query merge counters of the expert attention.
 __global__ void k_bucket_count(const int32_t* __restrict__ E, int N, int m, int s, int* __restrict__ counts,
-                               int use_smem, int* __restrict__ status) {
+                               int use_smem, int* __restrict__ cnt, int* __restrict__ status) {
     extern __shared__ int hist[];
     const int bh = blockIdx.y;
     if (use_smem) {
@@ -1051,6 +1087,7 @@ __global__ void k_bucket_count(const int32_t* __restrict__ E, int N, int m, int 
     }
     const int q = blockIdx.x * blockDim.x + threadIdx.x;
     if (q < N) {
+        cnt[(size_t)bh * N + q] = 0;
         for (int t = 0; t < s; ++t) {
             const int e = E[((size_t)bh * N + q) * s + t];
             if (e < 0 || e >= m) {
@@ -1071,9 +1108,11 @@ __global__ void k_bucket_count(const int32_t* __restrict__ E, int N, int m, int 
 
 // Per head: bucket offsets, scatter cursors and the head's work tiles
 // (x = head, y = expert, z = first bucket row, w = rows | shared_rows << 8).
+// xtl[bh * m + e] = (first tile, tile count) of each expert's bucket.
 __global__ void __launch_bounds__(512) k_bucket_scan(const int* __restrict__ counts, int m, int Ns,
                                                      int* __restrict__ cursors, int* __restrict__ toff,
-                                                     int* __restrict__ tile_ctr, int4* __restrict__ tiles) {
+                                                     int* __restrict__ tile_ctr, int4* __restrict__ tiles,
+                                                     int2* __restrict__ xtl) {
     __shared__ int tmp[33];
     __shared__ int sh_base;
     const int bh = blockIdx.x;
@@ -1101,6 +1140,7 @@ __global__ void __launch_bounds__(512) k_bucket_scan(const int* __restrict__ cou
         const int c0 = c[2 * e], n = c0 + c[2 * e + 1];
         const int start = cursors[((size_t)bh * m + e) * 2];
         const int t0 = base + toff[(size_t)bh * m + e];
+        xtl[(size_t)bh * m + e] = make_int2(t0, (n + kT - 1) / kT);
         for (int i = 0; i * kT < n; ++i) {
             const int rows = min(kT, n - i * kT);
             const int shr = max(0, min(rows, c0 - i * kT));
@@ -1607,24 +1647,26 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 
 // ------------------------------------------------------------------------
 // Expert attention with the expert's keys and values resident in shared
-// memory (k <= 256): each CTA walks a contiguous range of work tiles; the
-// tiles of one expert are adjacent, so K_(e), V_(e) are gathered once per
-// expert and reused by all its tiles. The shared slots come in as a separate
-// partial (routing kernel). The probabilities are written over the scores in
-// TMEM and O += P V reads them from there.
+// memory (k <= 256, m <= 128). Persistent, one CTA per SM. The CTAs claim
+// whole experts (all tiles of one (head, expert) bucket) from a counter, in
+// head order: the load stays balanced, an expert's keys and values are
+// gathered once for all its tiles, and at any moment all SMs work on about
+// one head. The shared slots come in as a separate partial (routing kernel);
+// the merge kernel combines the partials. The probabilities are written over
+// the scores in TMEM and O += P V reads them from there.
 //
-// Chunk stream: chunk g is key chunk c = g % nex of tile g / nex. The MMA
-// warp keeps S of chunks g and g + 1 in flight while the softmax works on g
-// (S of g + 2 goes right after O += P V of g, into the buffer P of g held),
-// except across a change of resident keys, where the old keys' last O += P V
-// goes first. The softmax warps defer a tile's epilogue until they have done
-// the next tile's first chunk, so the last O += P V of a tile is never waited
-// for. Each warp stages 16 rows at a time in shared memory, so that a store
-// instruction writes whole 128-byte halves of four partial rows.
+// Chunk stream: chunk g is key chunk c = g % nex of the CTA's tile g / nex.
+// The MMA warp keeps S of chunks g and g + 1 in flight while the softmax
+// works on g (S of g + 2 goes right after O += P V of g, into the buffer P
+// of g held), except across a change of resident keys, where the old keys'
+// last O += P V goes first. The softmax warps defer a tile's epilogue until
+// they have done the next tile's first chunk, so the last O += P V of a tile
+// is never waited for. Each warp stages 16 rows at a time in shared memory,
+// so that a store instruction writes whole 128-byte halves of four partial
+// rows.
 struct ResTile {
-    int bh, e, start, rows, gen;  // gen: loads of the resident keys so far (this tile uses load gen - 1)
+    int bh, e, start, rows, gen;  // gen: loads of the resident keys so far (this tile uses load gen - 1); rows < 0: end
 };
-
 
 // expert attention with resident keys: warps 0-7 softmax + epilogue,
 // 8 .. 8 + kNPW - 1 producers, then the MMA warp
@@ -1634,8 +1676,9 @@ template <int D>
 __global__ void __launch_bounds__(kResThreads, 1)
     k_expert_res(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
                  const __nv_bfloat16* __restrict__ V, const int32_t* __restrict__ I, const int32_t* __restrict__ perm,
-                 const int4* __restrict__ tiles, const int* __restrict__ tile_ctr, __nv_bfloat16* __restrict__ part,
-                 float* __restrict__ lse, int N, int m, int k, int s, float sl, int* __restrict__ status) {
+                 const int4* __restrict__ tiles, const int2* __restrict__ xtl, int nx, int* __restrict__ work_ctr,
+                 __nv_bfloat16* __restrict__ part, float* __restrict__ lse, int N, int m, int k, int s, float sl,
+                 int stall, int* __restrict__ status) {
     constexpr int TILE = kT * D * 2;
     constexpr uint32_t kS0 = 0, kO0 = 256;  // TMEM: S/P buffers 0 / 128, O buffers 256 / 384
     extern __shared__ uint8_t smem_raw[];
@@ -1646,8 +1689,10 @@ __global__ void __launch_bounds__(kResThreads, 1)
     uint8_t* sStage = sm + 6 * TILE;  // 8 x kStageWarp epilogue staging
 
     __shared__ uint64_t q_full[2], q_empty[2], kv_full[2], kv_rel[2], s_full[2], p_full[2], o_full[2], o_free[2];
-    __shared__ uint64_t pv_done;
+    __shared__ uint64_t pv_done, drain;
     __shared__ ResTile tinfo[2];
+    __shared__ int4 pnext[2];    // producer warp 0 -> all producer warps: the tile to load (w < 0: none)
+    __shared__ int pstop;        // producer warp 0 -> all producer warps: stop (a wait failed)
     __shared__ int rowq[2][kT];  // q << 3 | slot of each tile row, -1 past the tile's rows
     __shared__ int keyrow[kT];
     __shared__ float xmax[2][2][kT], xl[2][2][kT];  // [parity][half][row] exchange of the two softmax halves
@@ -1655,13 +1700,9 @@ __global__ void __launch_bounds__(kResThreads, 1)
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     volatile int* abort_v = &abort_flag;
+    const long long lim = stall ? kSpinTest : kSpin;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ntiles = *(volatile const int*)tile_ctr;
-    const int per = (ntiles + gridDim.x - 1) / gridDim.x;
-    const int t_begin = blockIdx.x * per, t_end = min(ntiles, t_begin + per);
-    const int nloc = max(0, t_end - t_begin);
-    if (nloc == 0) return;
     const int nex = (k + kT - 1) / kT;  // <= 2
     if (warp == 8 + kNPW) tmem_alloc(&tmem_slot, 512);
     if (threadIdx.x == 0) {
@@ -1676,6 +1717,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
             mbar_init(&o_free[i], 8);
         }
         mbar_init(&pv_done, 1);
+        mbar_init(&drain, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&xbar[i], 8);
             mbar_init(&ebar[i], 8);
@@ -1691,30 +1733,86 @@ __global__ void __launch_bounds__(kResThreads, 1)
 
     if (warp >= 8 && warp < 8 + kNPW) {
         // ------------------------------------------------------- producers
-        // all kNPW warps gather the tile's query rows and the resident keys /
-        // values (row pairs dealt round-robin); the first also writes tinfo
+        // Warp 0 claims the work and hands each tile to all producer warps
+        // (named barrier 1); all kNPW warps gather the tile's query rows and
+        // the resident keys / values (row pairs dealt round-robin). The index
+        // loads of the next tile (its bucket rows, and the expert's key
+        // indices when the expert changes) are issued one tile ahead, so that
+        // no gather waits on a dependent global load.
         const int pw = warp - 8;
         int cur_bh = -1, cur_e = -1, gen = 0;
+        int x_t = 0, x_end = 0;         // warp 0, lane 0: tiles left of the claimed expert
+        bool stall_pending = false;     // fault test: this CTA's first tile goes unpublished
         const int cc = lane % CPR;
-        for (int tl = 0; tl < nloc; ++tl) {
+        // warp 0, lane 0: the next tile of the claimed work (w < 0: none left)
+        auto next_tile = [&]() -> int4 {
+            int4 td = make_int4(0, 0, 0, -1);
+            if (*abort_v) return td;
+            while (x_t >= x_end) {
+                const int x = atomicAdd(work_ctr, 1);
+                if (x >= nx) return td;
+                if (x == 0 && stall) stall_pending = true;
+                const int2 r = xtl[x];
+                x_t = r.x;
+                x_end = r.x + r.y;
+            }
+            return tiles[x_t++];
+        };
+        // this lane's rows of a tile: r = lane + 32 i, the ones dealt to this warp
+        auto own = [&](int r) { return ((r / RPI) % kNPW) == pw; };
+        int pkv[kT / 32];        // bucket entries (q << 3 | slot) of the next tile's rows, -1 for none
+        int krv[2][kT / 32];     // key indices of the next expert's rows (when it changes)
+        auto prefetch = [&](const int4& td) {
+            const int rows = td.w & 255;
+            const int32_t* pb = perm + (size_t)td.x * N * s + td.z;
+#pragma unroll
+            for (int i = 0; i < kT / 32; ++i) {
+                const int r = lane + 32 * i;
+                pkv[i] = (td.w >= 0 && own(r) && r < rows) ? pb[r] : -1;
+            }
+            if (td.w >= 0 && (td.x != cur_bh || td.y != cur_e)) {
+                const int32_t* Ie = I + ((size_t)td.x * m + td.y) * k;
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int i = 0; i < kT / 32; ++i) {
+                        const int t2 = c * kT + lane + 32 * i;
+                        krv[c][i] = (c < nex && own(lane + 32 * i) && t2 < k) ? Ie[t2] : 0;
+                    }
+            }
+        };
+        if (pw == 0 && lane == 0) pnext[0] = next_tile();
+        named_sync(1, 32 * kNPW);
+        int4 td = pnext[0];
+        prefetch(td);
+        for (int tl = 0;; ++tl) {
             const int qs = tl & 1;
-            const int4 td = tiles[t_begin + tl];
+            // the slot is free (warp 0 waits, then tells the others)
+            if (pw == 0 && lane == 0)
+                pstop = !ws_wait(&q_empty[qs], ((tl >> 1) & 1) ^ 1, status, abort_v, lim) || *abort_v;
+            named_sync(1, 32 * kNPW);
+            if (pstop) break;
+            if (td.w < 0) {
+                // no more work: an end marker for the consumers, in the free slot
+                if (pw == 0 && lane == 0) tinfo[qs] = ResTile{0, 0, 0, -1, 0};
+                cp_async_arrive(&q_full[qs]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&q_full[qs]);
+                break;
+            }
             const int bh = td.x, e = td.y, start = td.z, rows = td.w & 255;
             const bool reload = bh != cur_bh || e != cur_e;
-            {
-                int ok = 1;
-                if (lane == 0) ok = ws_wait(&q_empty[qs], ((tl >> 1) & 1) ^ 1, status, abort_v);
-                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            }
-            // this warp's rows: (query, slot) from the bucket order, -1 past the tile's rows
-            for (int r = lane; r < kT; r += 32) {
-                if ((r / RPI) % kNPW != pw) continue;
-                int pk = r < rows ? perm[(size_t)bh * N * s + start + r] : -1;
+            (void)start;
+#pragma unroll
+            for (int i = 0; i < kT / 32; ++i) {
+                const int r = lane + 32 * i;
+                if (!own(r)) continue;
+                int pk = pkv[i];
                 if (pk >= 0 && (pk >> 3) >= N) {
                     set_status(status, kStBounds);
                     pk = -1;
                 }
-                rowq[qs][r] = pk;
+                rowq[qs][r] = r < rows ? pk : -1;
             }
             if (pw == 0 && lane == 0) tinfo[qs] = ResTile{bh, e, start, rows, gen + (reload ? 1 : 0)};
             __syncwarp();
@@ -1728,25 +1826,29 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 }
                 cp_async_arrive(&q_full[qs]);  // counts once this thread's copies have landed
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&q_full[qs]);  // publishes this warp's rowq rows (and tinfo)
+                // publishes this warp's rowq rows (and tinfo); the fault test
+                // leaves one arrival out, so the consumers' bounded waits run out
+                const bool skip = stall_pending && pw == 0;
+                stall_pending = false;
+                if (lane == 0 && !skip) mbar_arrive(&q_full[qs]);
             }
             if (reload) {
                 const __nv_bfloat16* Kb = K + (size_t)bh * N * D;
                 const __nv_bfloat16* Vb = V + (size_t)bh * N * D;
-                const int32_t* Ie = I + ((size_t)bh * m + e) * k;
                 bool okc = true;
                 for (int c = 0; c < nex; ++c) {
                     // every MMA on the previous keys of this chunk is done: the MMA
                     // warp commits kv_rel[c] once per change of keys (gen - 1 so far)
                     if (gen > 0) {
                         int okw = 1;
-                        if (lane == 0) okw = ws_wait(&kv_rel[c], (gen - 1) & 1, status, abort_v);
+                        if (lane == 0) okw = ws_wait(&kv_rel[c], (gen - 1) & 1, status, abort_v, lim);
                         if (!__shfl_sync(0xffffffffu, okw, 0)) { okc = false; break; }
                     }
-                    for (int r = lane; r < kT; r += 32) {  // this warp's rows only
-                        if ((r / RPI) % kNPW != pw) continue;
-                        const int t2 = c * kT + r;
-                        int j = t2 < k ? Ie[t2] : 0;
+#pragma unroll
+                    for (int i = 0; i < kT / 32; ++i) {
+                        const int r = lane + 32 * i;
+                        if (!own(r)) continue;
+                        int j = krv[c][i];
                         if (j < 0 || j >= N) {
                             set_status(status, kStBounds);
                             j = 0;
@@ -1765,62 +1867,115 @@ __global__ void __launch_bounds__(kResThreads, 1)
                     cp_async_arrive(&kv_full[c]);
                     __syncwarp();
                 }
-                if (!okc) break;
-                ++gen;
-                cur_bh = bh;
-                cur_e = e;
+                // after a failed wait the abort flag is up: the next tile's
+                // slot wait hands every producer warp the stop
+                if (okc) {
+                    ++gen;
+                    cur_bh = bh;
+                    cur_e = e;
+                }
             }
+            // the next tile, and its index loads in flight while this one is consumed
+            if (pw == 0 && lane == 0) pnext[(tl + 1) & 1] = next_tile();
+            named_sync(1, 32 * kNPW);
+            td = pnext[(tl + 1) & 1];
+            prefetch(td);
         }
         cp_async_wait_all();  // nothing of ours may still be in flight when the CTA exits
     } else if (warp == 8 + kNPW) {
         // ------------------------------------------------------ MMA issuer
+        // One thread polls the barriers without blocking: O += P V of chunk g
+        // goes out as soon as its probabilities are in, and S of the next
+        // chunk as soon as its query tile and keys are; neither waits behind
+        // the other. S runs at most one chunk ahead of the last O += P V.
         if (lane == 0) {
-            const int G = nloc * nex;
+            int G = 0x7fffffff;    // chunks in all, known once the end marker is seen
+            int g = 0;             // next chunk whose O += P V is to be issued
             int ns = 0;            // next chunk whose S is to be issued
-            int seen_tl = -1;      // last tile whose query tile was waited for
-            int s_gen = 0, cur_gen = 0;  // keys of chunk ns's tile / of the last S issued
-            bool rel_last = false, ok = true;
-            for (int g = 0; g < G && ok; ++g) {
-                // S of chunks up to g + 1
-                while (ns <= g + 1 && ns < G) {
+            int seen_tl = -1;      // last tile whose query tile was seen
+            int s_gen = 0, cur_gen = 0;  // keys of chunk ns's tile / of the S issued last
+            bool rel_early = false;      // old keys' other chunks released, the last one pending
+            long long idle0 = clock64();
+            while (g < G) {
+                bool prog = false;
+                // ---- S of chunk ns
+                if (ns < G && ns <= g + 1) {
                     const int tl = ns / nex, c = ns - tl * nex, qs = tl & 1;
+                    bool ready = true;
                     if (tl != seen_tl) {
-                        if (!(ok = ws_wait(&q_full[qs], (tl >> 1) & 1, status, abort_v))) break;
-                        s_gen = tinfo[qs].gen;
-                        seen_tl = tl;
-                    }
-                    if (s_gen != cur_gen) {
-                        if (cur_gen > 0 && ns - 1 >= g) {
-                            // the old keys' last O += P V (chunk ns - 1) goes first; the
-                            // other chunks of the old keys are done with now
-                            for (int c2 = 0; c2 < nex - 1; ++c2) mma_commit(&kv_rel[c2]);
-                            rel_last = true;
-                            break;
+                        if (mbar_test_wait(&q_full[qs], (tl >> 1) & 1)) {
+                            seen_tl = tl;
+                            const ResTile ti = tinfo[qs];
+                            prog = true;
+                            if (ti.rows < 0) {
+                                G = ns;
+                                ready = false;
+                            } else {
+                                s_gen = ti.gen;
+                            }
+                        } else {
+                            ready = false;
                         }
-                        cur_gen = s_gen;
                     }
-                    if (!(ok = ws_wait(&kv_full[c], (s_gen - 1) & 1, status, abort_v))) break;
-                    fence_proxy_async();  // copied tiles (generic proxy) -> the MMA's async-proxy reads
-                    fence_after_sync();
-                    issue_qk<D>(tmem + kS0 + (ns & 1) * 128, smem_u32(sQ + qs * TILE), smem_u32(sK + c * TILE), false);
-                    mma_commit(&s_full[ns & 1]);
-                    if (c == nex - 1) mma_commit(&q_empty[qs]);
-                    ++ns;
+                    if (ready && s_gen != cur_gen) {
+                        if (cur_gen > 0) {
+                            // the old keys' other chunks are done with once their last
+                            // O += P V is issued (S runs at most one chunk ahead)
+                            if (!rel_early) {
+                                for (int c2 = 0; c2 < nex - 1; ++c2) mma_commit(&kv_rel[c2]);
+                                rel_early = true;
+                                prog = true;
+                            }
+                            if (g < ns) {
+                                ready = false;  // the old keys' last O += P V goes first
+                            } else {
+                                mma_commit(&kv_rel[nex - 1]);
+                                rel_early = false;
+                                cur_gen = s_gen;
+                            }
+                        } else {
+                            cur_gen = s_gen;
+                        }
+                    }
+                    if (ready && mbar_test_wait(&kv_full[c], (s_gen - 1) & 1)) {
+                        fence_proxy_async();  // copied tiles (generic proxy) -> the MMA's async-proxy reads
+                        fence_after_sync();
+                        issue_qk<D>(tmem + kS0 + (ns & 1) * 128, smem_u32(sQ + qs * TILE), smem_u32(sK + c * TILE),
+                                    false);
+                        mma_commit(&s_full[ns & 1]);
+                        if (c == nex - 1) mma_commit(&q_empty[qs]);
+                        ++ns;
+                        prog = true;
+                    }
                 }
-                if (!ok) break;
-                // O += P V of chunk g
-                const int tl = g / nex, c = g - tl * nex, ob = tl & 1;
-                if (!(ok = ws_wait(&p_full[g & 1], (g >> 1) & 1, status, abort_v))) break;
-                if (c == 0 && !(ok = ws_wait(&o_free[ob], ((tl >> 1) & 1) ^ 1, status, abort_v))) break;
-                fence_after_sync();
-                issue_pv_ts<D>(tmem + kO0 + ob * 128, tmem + kS0 + (g & 1) * 128, smem_u32(sV + c * TILE), c > 0);
-                mma_commit(&pv_done);
-                if (c == nex - 1) mma_commit(&o_full[ob]);
-                if (rel_last) {
-                    mma_commit(&kv_rel[nex - 1]);
-                    rel_last = false;
+                // ---- O += P V of chunk g
+                if (g < ns && g < G) {
+                    const int tl = g / nex, c = g - tl * nex, ob = tl & 1;
+                    if (mbar_test_wait(&p_full[g & 1], (g >> 1) & 1) &&
+                        (c != 0 || mbar_test_wait(&o_free[ob], ((tl >> 1) & 1) ^ 1))) {
+                        fence_after_sync();
+                        issue_pv_ts<D>(tmem + kO0 + ob * 128, tmem + kS0 + (g & 1) * 128, smem_u32(sV + c * TILE),
+                                       c > 0);
+                        mma_commit(&pv_done);
+                        if (c == nex - 1) mma_commit(&o_full[ob]);
+                        ++g;
+                        prog = true;
+                    }
+                }
+                if (prog) {
+                    idle0 = clock64();
+                } else {
+                    if (*abort_v) break;
+                    if (clock64() - idle0 > lim) {
+                        set_status(status, kStTimeout);
+                        *abort_v = 1;
+                        break;
+                    }
                 }
             }
+            // every MMA this thread issued has completed before TMEM is freed
+            mma_commit(&drain);
+            drain_wait(&drain, 0, status);
         }
         __syncwarp();
     } else {
@@ -1833,13 +1988,15 @@ __global__ void __launch_bounds__(kResThreads, 1)
         const bool fast = sl > 0.0f;  // the row max of the scaled scores is the scaled max
         uint8_t* stage = sStage + warp * kStageWarp;
         // epilogue of tile pt: normalized bf16 partial rows (row pk >> 3, slot
-        // pk & 7 of head pti.bh) and their log2-sum-exp
+        // pk & 7 of head pti.bh) and their log2-sum-exp, then the count and,
+        // for the queries whose last half row this is, the merge
         // plt: the whole row sum when the two halves already exchanged it (with the
-        // next tile's first row maxima), else < 0 and the epilogue exchanges it
-        auto epilogue = [&](int pt, const ResTile& pti, int pk, float pl, float pm, float plt) -> bool {
+        // next tile's first row maxima); last: the CTA's last tile, whose
+        // epilogue exchanges the row sum itself
+        auto epilogue = [&](int pt, const ResTile& pti, int pk, float pl, float pm, float plt, bool last) -> bool {
             constexpr int PPR = DH / 8, RPI = 32 / PPR;  // pieces per half row, rows per store instruction
             const int ob = pt & 1;
-            if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (pt >> 1) & 1, status, abort_v))) return false;
+            if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (pt >> 1) & 1, status, abort_v, lim))) return false;
             fence_after_sync();
             const uint32_t tO = lane_base(tmem) + kO0 + ob * 128 + wg * DH;
             float o[DH];
@@ -1847,12 +2004,12 @@ __global__ void __launch_bounds__(kResThreads, 1)
             for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(tO + c0, o + c0);
             tmem_wait_ld();
             float lt = plt;
-            if (plt < 0.0f) {  // the CTA's last tile: one exchange of its own (ebar's only use)
+            if (last) {  // the CTA's last tile: one exchange of its own (ebar's only use)
                 xl[pt & 1][wg][r] = pl;
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ebar[0]);
-                if (!__all_sync(0xffffffffu, ws_wait(&ebar[0], 0, status, abort_v))) return false;
+                if (!__all_sync(0xffffffffu, ws_wait(&ebar[0], 0, status, abort_v, lim))) return false;
                 lt = pl + xl[pt & 1][wg ^ 1][r];
             } else {
                 fence_before_sync();
@@ -1891,10 +2048,15 @@ __global__ void __launch_bounds__(kResThreads, 1)
         ResTile pti{};
         int ppk = -1;
         float pl = 0.0f, pm = 0.0f;
-        for (int tl = 0; tl < nloc && ok; ++tl) {
+        int tl = 0;
+        for (;; ++tl) {
             const int qs = tl & 1, ob = tl & 1;
-            if (!__all_sync(0xffffffffu, ws_wait(&q_full[qs], (tl >> 1) & 1, status, abort_v))) break;
+            if (!__all_sync(0xffffffffu, ws_wait(&q_full[qs], (tl >> 1) & 1, status, abort_v, lim))) {
+                ok = false;
+                break;
+            }
             const ResTile ti = tinfo[qs];
+            if (ti.rows < 0) break;  // end of the work
             const int pk = rowq[qs][r];
             __syncwarp();
             if (lane == 0) mbar_arrive(&q_empty[qs]);  // tinfo / rowq read; the MMA releases the tile itself
@@ -1903,7 +2065,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
             const uint32_t tO = lane_base(tmem) + kO0 + ob * 128 + wg * DH;
             for (int c = 0; c < nex; ++c, ++g) {
                 const int sb = g & 1;
-                if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (g >> 1) & 1, status, abort_v))) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (g >> 1) & 1, status, abort_v, lim))) { ok = false; break; }
                 fence_after_sync();
                 const uint32_t tS = lane_base(tmem) + kS0 + sb * 128;
                 const int nval = valid ? min(kT, k - c * kT) - 64 * wg : 0;  // valid columns of this half
@@ -1927,7 +2089,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&xbar[g & 1]);
                 // both halves have read S(g) and posted their max (bounded wait)
-                if (!__all_sync(0xffffffffu, ws_wait(&xbar[g & 1], (g >> 1) & 1, status, abort_v))) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, ws_wait(&xbar[g & 1], (g >> 1) & 1, status, abort_v, lim))) { ok = false; break; }
                 fence_after_sync();
                 mx = fmaxf(mx, xmax[g & 1][wg ^ 1][r]);
                 float mnew = mref, alpha = 1.0f;
@@ -1961,7 +2123,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 if (__any_sync(0xffffffffu, c > 0 && alpha != 1.0f)) {
                     // S(g) done implies O += P V of chunk g - 2 done: this wait can only
                     // see chunk g - 1's phase
-                    if (!__all_sync(0xffffffffu, ws_wait(&pv_done, (g - 1) & 1, status, abort_v))) { ok = false; break; }
+                    if (!__all_sync(0xffffffffu, ws_wait(&pv_done, (g - 1) & 1, status, abort_v, lim))) { ok = false; break; }
                     fence_after_sync();
                     const float a = (c > 0) ? alpha : 1.0f;
 #pragma unroll 1
@@ -1981,7 +2143,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 // the previous tile's epilogue, now that its last O += P V has had a chunk's time
                 if (c == 0 && have_prev) {
                     // the other half posted its share before this chunk's exchange
-                    if (!(ok = epilogue(tl - 1, pti, ppk, pl, pm, pl + xl[(tl - 1) & 1][wg ^ 1][r]))) break;
+                    if (!(ok = epilogue(tl - 1, pti, ppk, pl, pm, pl + xl[(tl - 1) & 1][wg ^ 1][r], false))) break;
                     have_prev = false;
                 }
             }
@@ -1992,7 +2154,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
             pl = l;
             pm = mref;
         }
-        if (ok && have_prev) epilogue(nloc - 1, pti, ppk, pl, pm, -1.0f);
+        if (ok && have_prev) epilogue(tl - 1, pti, ppk, pl, pm, 0.0f, true);
     }
     fence_before_sync();
     __syncthreads();
@@ -2141,7 +2303,9 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
                                 cudaStream_t st) {
     const __nv_bfloat16* q = (const __nv_bfloat16*)Q;
     const __nv_bfloat16* kk = (const __nv_bfloat16*)K;
-    const __nv_bfloat16* v = (const __nv_bfloat16*)V;
+    // mita_select passes no V: the landmark pass still runs its P V MMAs (their
+    // result, the shared expert, is not used then) and reads K in V's place
+    const __nv_bfloat16* v = (const __nv_bfloat16*)(V ? V : K);
     const float sl = D.scale * 1.4426950408889634f;
     const int tile = kT * DD * 2;
     cudaError_t e;
@@ -2170,7 +2334,8 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
         if ((e = set_smem(k_landmark_ws<DD, NS>, smem))) return e;
         dim3 grid(P.m_tiles, P.splits, D.BH);
         k_landmark_ws<DD, NS><<<grid, 320, smem, st>>>(mk, mv, W.Qhi, W.Qlo, W.thr, W.cand, W.ccount, W.Opart, W.ML,
-                                                      D.N, D.m, P.m_pad, P.splits, P.chunks_per_split, sl, status);
+                                                      D.N, D.m, P.m_pad, P.splits, P.chunks_per_split, sl,
+                                                      (D.flags & MITA_TESTFLAG_STALL_PRODUCER) ? 1 : 0, status);
         if ((e = cudaGetLastError())) return e;
         count_launch();
     }
@@ -2196,20 +2361,23 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
     {
         const int use_smem = D.m <= 4096;
         dim3 grid((D.N + 255) / 256, D.BH);
-        k_bucket_count<<<grid, 256, use_smem ? 8 * D.m : 0, st>>>(E, D.N, D.m, D.s, W.counts, use_smem, status);
-        k_bucket_scan<<<D.BH, 512, 0, st>>>(W.counts, D.m, D.N * D.s, W.cursors, W.toff, W.tile_ctr, W.tiles);
+        k_bucket_count<<<grid, 256, use_smem ? 8 * D.m : 0, st>>>(E, D.N, D.m, D.s, W.counts, use_smem, W.cnt,
+                                                                  status);
+        k_bucket_scan<<<D.BH, 512, 0, st>>>(W.counts, D.m, D.N * D.s, W.cursors, W.toff, W.tile_ctr, W.tiles,
+                                            W.xtl);
         k_bucket_scatter<<<grid, 256, use_smem ? 8 * D.m : 0, st>>>(E, D.N, D.m, D.s, W.cursors, W.perm, use_smem);
         if ((e = cudaGetLastError())) return e;
         count_launch(3);
     }
     // expert attention + merge
-    prof_mark(st, "expert");
     {
         if (P.resident) {
+            prof_mark(st, "expert_res");
             const int smem = 6 * tile + 8 * kStageWarp + 1024;
             if ((e = set_smem(k_expert_res<DD>, smem))) return e;
-            k_expert_res<DD><<<num_sms(), kResThreads, smem, st>>>(q, kk, v, I, W.perm, W.tiles, W.tile_ctr, W.part,
-                                                                   W.lse, D.N, D.m, D.k, D.s, sl, status);
+            k_expert_res<DD><<<num_sms(), kResThreads, smem, st>>>(
+                q, kk, v, I, W.perm, W.tiles, W.xtl, D.BH * D.m, W.tile_ctr + 1, W.part, W.lse, D.N, D.m, D.k, D.s,
+                sl, (D.flags & MITA_TESTFLAG_STALL_PRODUCER) ? 1 : 0, status);
             if ((e = cudaGetLastError())) return e;
             count_launch();
             prof_mark(st, "merge");
@@ -2217,6 +2385,7 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
             k_merge<DD><<<(unsigned)((nq * (DD / 8) + 255) / 256), 256, 0, st>>>(W.part, W.lse, W.sh_part, W.sh_lse,
                                                                                (__nv_bfloat16*)O, nq, D.s);
         } else {
+            prof_mark(st, "expert_ws");
             const int smem = 4 * tile + 2 * kp_bytes<DD>() + 1024;
             if ((e = set_smem(k_expert_ws<DD>, smem))) return e;
             k_expert_ws<DD><<<num_sms(), kWsThreads, smem, st>>>(q, kk, v, W.Qhi, W.Vtb, I, W.perm, W.tiles,

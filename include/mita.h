@@ -72,6 +72,19 @@ enum {
     MITA_FLAG_SIMT = 1u << 1
 };
 
+/* Fault test of the device-side failure detection, not for production: in
+ * one CTA of the landmark pass and one of the expert attention, a producer
+ * leaves out one of the signals its consumers wait for, and every bounded
+ * wait of those two kernels gives up after about a millisecond instead of a
+ * second. The call then records MITA_ERR_TIMEOUT in the device status word
+ * (read with mita_device_status()); every role of the stalled CTAs leaves its
+ * loop, lets its copies and MMAs in flight land and frees its tensor memory,
+ * so the next call on the same workspace runs normally. Outputs of the
+ * flagged call are undefined. Only the tensor-core path has these waits: on
+ * the CUDA-core path the flag has no effect. (A macro, since the bit is
+ * outside the int range of a C enum constant.) */
+#define MITA_TESTFLAG_STALL_PRODUCER (1u << 31)
+
 typedef struct {
     int B, H, N, d;   /* batch, heads, tokens, head dim (8 <= d <= 256, d % 8 == 0) */
     int m, k, s;      /* landmarks (1..N), top-k width (1..N), routed experts (1..min(m, 8)) */

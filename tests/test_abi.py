@@ -63,3 +63,13 @@ def test_host_side_errors_are_synchronous(lib):
     for s in range(7):
         assert lib.mita_status_string(s)
     assert mita.mita_host_buffer_size(p) > mita.mita_workspace_size(p)
+
+
+def test_flag_values_match_the_header(lib):
+    src = open(os.path.join(ROOT, "include", "mita.h")).read()
+    assert re.search(r"MITA_FLAG_NO_SHARED\s*=\s*1u\s*<<\s*0\b", src) and mita.FLAG_NO_SHARED == 1
+    assert re.search(r"MITA_FLAG_SIMT\s*=\s*1u\s*<<\s*1\b", src) and mita.FLAG_SIMT == 2
+    assert re.search(r"#define\s+MITA_TESTFLAG_STALL_PRODUCER\s+\(1u\s*<<\s*31\)", src)
+    assert mita.TESTFLAG_STALL_PRODUCER == 1 << 31
+    # the fault-test flag is a valid flag (accepted on the host, like the others)
+    assert mita.mita_workspace_size(_p(flags=mita.TESTFLAG_STALL_PRODUCER)) > 0
