@@ -33,6 +33,7 @@ class MoParams(ctypes.Structure):
         ("grid_h", ctypes.c_int), ("grid_w", ctypes.c_int),
         ("lm_h", ctypes.c_int), ("lm_w", ctypes.c_int),
         ("scale", ctypes.c_double), ("no_shared", ctypes.c_int),
+        ("causal", ctypes.c_int),
     ]
 
 
@@ -71,10 +72,10 @@ def _ip(a):
     return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
 
 
-def _params(N, d, m, k, s, grid=None, lm=None, scale=0.0, no_shared=False):
+def _params(N, d, m, k, s, grid=None, lm=None, scale=0.0, no_shared=False, causal=False):
     gh, gw = grid if grid else (1, N)
     lh, lw = lm if lm else (1, m)
-    return MoParams(N, d, m, k, s, gh, gw, lh, lw, float(scale), int(bool(no_shared)))
+    return MoParams(N, d, m, k, s, gh, gw, lh, lw, float(scale), int(bool(no_shared)), int(bool(causal)))
 
 
 def _f64(a):
@@ -101,15 +102,20 @@ def scores(A, B):
 
 
 def forward(Q, K, V, m, k, s, grid=None, lm=None, scale=0.0, no_shared=False, q_ids=None,
-            I_override=None, E_override=None, threads=None):
+            I_override=None, E_override=None, threads=None, causal=False):
     """MiTA forward for independent heads: Q, K, V [H, N, d] (float64).
+
+    causal=True is this build's causal variant (1-D pooling only; the rules are
+    in the header of mita_oracle.c): Vt_i over the keys of landmark i's prefix,
+    a landmark's shared slot only once its bin is complete, routed keys up to
+    the query's own position, zero output for a query with no slot.
 
     Returns a dict with Qt, Vt [H, m, d], I [H, m, k] (ascending), E [H, n_q, s]
     (descending routing score), O [H, n_q, d] and the multiply-add count.
     """
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     H, N, d = Q.shape
-    p = _params(N, d, m, k, s, grid, lm, scale, no_shared)
+    p = _params(N, d, m, k, s, grid, lm, scale, no_shared, causal)
     if q_ids is None:
         n_q, qp = N, None
     else:

@@ -33,6 +33,16 @@
  *   - adaptive pooling bins are [floor(i*N/m), ceil((i+1)*N/m)) per axis;
  *   - one joint softmax over all m + s*k slots, non-causal.
  *
+ * Causal variant (causal = 1; the summaries do not describe one, so every
+ * rule below is a reading of this build, for 1-D pooling only):
+ *   - the shared expert of landmark i attends to the keys of its prefix only,
+ *     Vt_i = softmax over j < hi_i, where [lo_i, hi_i) is landmark i's bin;
+ *   - query t has the shared slot of landmark i only once that bin is
+ *     complete, hi_i <= t + 1;
+ *   - expert sets and routes are selected as in the non-causal pass; of a
+ *     routed expert's keys, query t attends to those with j <= t;
+ *   - a query left with no slot gets a zero output row.
+ *
  * Pins: see tests/test_oracle_pins.py (closed forms, brute force, library
  * special cases, a hand-derived example).
  */
@@ -48,6 +58,7 @@ typedef struct {
     int lm_h, lm_w;     /* landmark grid; lm_h == 1 means 1D               */
     double scale;       /* <= 0 means 1/sqrt(d)                             */
     int no_shared;      /* 1: drop the m shared slots from step 5           */
+    int causal;         /* 1: the causal variant (1-D pooling only)         */
 } mo_params;
 
 /* ---------------------------------------------------------------- step 1 */
@@ -144,18 +155,28 @@ static void mo_run_head(mo_job* jb) {
             if (tau * srow[j] > mx) mx = tau * srow[j];
         }
         macs += (uint64_t)N * d;
-        /* Vt_i = sum_j softmax_j(tau s_ij) v_j, max-subtracted */
+        /* Vt_i = sum_j softmax_j(tau s_ij) v_j, max-subtracted; the causal
+         * variant keeps the keys of landmark i's prefix, j < hi_i */
+        int jend = N;
+        if (p->causal) {
+            int lo, hi;
+            mo_bin(i, N, m, &lo, &hi);
+            jend = hi;
+            mx = -INFINITY;
+            for (int j = 0; j < jend; ++j)
+                if (tau * srow[j] > mx) mx = tau * srow[j];
+        }
         double* vt = jb->Vt + (size_t)i * d;
         for (int c = 0; c < d; ++c) vt[c] = 0.0;
         double den = 0.0;
-        for (int j = 0; j < N; ++j) {
+        for (int j = 0; j < jend; ++j) {
             double w = exp(tau * srow[j] - mx);
             den += w;
             const double* v = jb->V + (size_t)j * d;
             for (int c = 0; c < d; ++c) vt[c] += w * v[c];
         }
         for (int c = 0; c < d; ++c) vt[c] /= den;
-        macs += (uint64_t)N * d;
+        macs += (uint64_t)jend * d;
         /* I_i: first k of (score desc, index asc), then ascending index */
         int32_t* Ii = jb->I + (size_t)i * k;
         if (jb->I_over) {
@@ -189,19 +210,32 @@ static void mo_run_head(mo_job* jb) {
             qsort(r, (size_t)m, sizeof(mo_item), mo_cmp_desc);
             for (int e = 0; e < s; ++e) Et[e] = r[e].j;
         }
-        /* step 5: K* = [Qt, K_(e1), ..., K_(es)], V* = [Vt, V_(e1), ...] */
+        /* step 5: K* = [Qt, K_(e1), ..., K_(es)], V* = [Vt, V_(e1), ...];
+         * the causal variant drops the landmarks whose bin is not complete at
+         * qi and the routed keys after qi */
         int n = 0;
         if (!p->no_shared)
             for (int i = 0; i < m; ++i) {
+                if (p->causal) {
+                    int lo, hi;
+                    mo_bin(i, N, m, &lo, &hi);
+                    if (hi > qi + 1) continue;
+                }
                 logit[n] = tau * mo_dot(q, jb->Qt + (size_t)i * d, d);
                 vals[n++] = jb->Vt + (size_t)i * d;
             }
         for (int e = 0; e < s; ++e) {
             const int32_t* Ie = jb->I + (size_t)Et[e] * k;
             for (int t2 = 0; t2 < k; ++t2) {
+                if (p->causal && Ie[t2] > qi) continue;
                 logit[n] = tau * mo_dot(q, jb->K + (size_t)Ie[t2] * d, d);
                 vals[n++] = jb->V + (size_t)Ie[t2] * d;
             }
+        }
+        if (n == 0) {  /* causal only: no slot at all */
+            double* o = jb->O + (size_t)t * d;
+            for (int c = 0; c < d; ++c) o[c] = 0.0;
+            continue;
         }
         double mx = -INFINITY;
         for (int u = 0; u < n; ++u) if (logit[u] > mx) mx = logit[u];
@@ -247,6 +281,7 @@ static int mo_check(const mo_params* p) {
     if (p->grid_h < 1 || p->grid_w < 1 || p->grid_h * p->grid_w != p->N) return -1;
     if (p->lm_h < 1 || p->lm_w < 1 || p->lm_h * p->lm_w != p->m) return -1;
     if (p->lm_h > p->grid_h || p->lm_w > p->grid_w) return -1;
+    if (p->causal && p->grid_h != 1) return -1; /* causal: 1-D token order only */
     return 0;
 }
 

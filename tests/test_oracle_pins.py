@@ -266,3 +266,96 @@ def test_rejects_bad_parameters():
         oracle.forward(Q, Q, Q, m=2, k=9, s=1)
     with pytest.raises(ValueError):
         oracle.forward(Q, Q, Q, m=2, k=1, s=3)
+
+
+# ------------------------------------------------------- causal variant
+# The pages describe no causal form; this build's reading (1-D pooling):
+# Vt_i over the keys of landmark i's prefix (j < hi_i), a shared slot only once
+# the landmark's bin is complete (hi_i <= t + 1), routed keys up to the query's
+# position (j <= t), zero output when a query has no slot.
+
+def _bins_hi(N, m):
+    return np.array([-(-(i + 1) * N // m) for i in range(m)])  # ceil((i + 1) N / m)
+
+
+@pytest.mark.parametrize("scale", [0.0, 0.3])
+def test_causal_no_shared_full_k_is_causal_softmax_attention(scale):
+    N, d, m = 96, 8, 6
+    Q, K, V = (_rand((2, N, d), 40 + i) for i in range(3))
+    r = oracle.forward(Q, K, V, m=m, k=N, s=1, scale=scale, no_shared=True, causal=True, threads=2)
+    t = lambda a: torch.from_numpy(a)
+    ref = torch.nn.functional.scaled_dot_product_attention(t(Q), t(K), t(V), is_causal=True,
+                                                           scale=scale if scale > 0 else None).numpy()
+    np.testing.assert_allclose(r["O"], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_causal_shared_full_k_is_masked_attention_over_landmarks_and_keys():
+    # every key in every expert (k = N, s = 1): query t attends to the landmarks
+    # of complete bins (values: attention of the landmark over its prefix) and
+    # to the keys up to t, in one softmax; built here from library pooling and
+    # masked SDPA
+    N, d, m = 64, 5, 8
+    Q, K, V = (_rand((1, N, d), 50 + i) for i in range(3))
+    r = oracle.forward(Q, K, V, m=m, k=N, s=1, causal=True, threads=1)
+    tq, tk, tv = (torch.from_numpy(a[0]) for a in (Q, K, V))
+    Qt = torch.nn.functional.adaptive_avg_pool1d(tq.T[None], m)[0].T
+    hi = _bins_hi(N, m)
+    key_mask = torch.arange(N)[None, :] < torch.from_numpy(hi)[:, None]        # [m, N]: j < hi_i
+    Vt = torch.nn.functional.scaled_dot_product_attention(Qt[None], tk[None], tv[None], attn_mask=key_mask[None])[0]
+    np.testing.assert_allclose(r["Vt"][0], Vt.numpy(), rtol=1e-12, atol=1e-12)
+    keys = torch.cat([Qt, tk])
+    vals = torch.cat([Vt, tv])
+    pos = torch.arange(N)[:, None]
+    mask = torch.cat([torch.from_numpy(hi)[None, :] <= pos + 1, torch.arange(N)[None, :] <= pos], dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq[None], keys[None], vals[None], attn_mask=mask[None])[0]
+    np.testing.assert_allclose(r["O"][0], ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_causal_output_ignores_later_positions():
+    # with every key in every expert, routes do not matter, and the output at t
+    # depends on positions <= t only: changing the later ones leaves it alone
+    N, d, m = 80, 4, 5
+    Q, K, V = (_rand((1, N, d), 60 + i) for i in range(3))
+    base = oracle.forward(Q, K, V, m=m, k=N, s=2, causal=True, threads=1)["O"][0]
+    for t in (0, 15, 16, 47, 79):
+        Q2, K2, V2 = Q.copy(), K.copy(), V.copy()
+        rng = np.random.default_rng(t)
+        for a in (Q2, K2, V2):
+            a[0, t + 1:] = rng.standard_normal(a[0, t + 1:].shape)
+        got = oracle.forward(Q2, K2, V2, m=m, k=N, s=2, causal=True, threads=1)["O"][0]
+        np.testing.assert_allclose(got[:t + 1], base[:t + 1], rtol=1e-13, atol=1e-13)
+
+
+def test_causal_query_without_slots_is_zero():
+    # N = 8, m = 2 (bins [0, 4), [4, 8)), k = s = 1: key 7 is every landmark's
+    # top key. Query 0 has no complete bin and its only routed key is later:
+    # no slot, zero output. Query 3 completes bin 0: its only slot is
+    # landmark 0, so its output is Vt_0 (attention of qt_0 over keys 0..3).
+    N, d = 8, 2
+    K = np.zeros((1, N, d)); K[0, 7] = [5.0, 5.0]
+    Q = np.ones((1, N, d))
+    V = _rand((1, N, d), 70)
+    r = oracle.forward(Q, K, V, m=2, k=1, s=1, causal=True, threads=1)
+    assert np.array_equal(r["I"][0], [[7], [7]])
+    np.testing.assert_array_equal(r["O"][0, 0], np.zeros(d))
+    np.testing.assert_allclose(r["Vt"][0, 0], V[0, :4].mean(axis=0), rtol=1e-14)  # equal scores: plain mean
+    np.testing.assert_allclose(r["O"][0, 3], r["Vt"][0, 0], rtol=1e-14)
+
+
+def test_causal_last_landmark_and_sets_match_noncausal():
+    # the last bin ends at N, so its prefix is every key; sets and routes are
+    # selected as in the non-causal pass
+    N, d, m = 120, 6, 4
+    Q, K, V = (_rand((1, N, d), 80 + i) for i in range(3))
+    a = oracle.forward(Q, K, V, m=m, k=17, s=2, threads=1)
+    b = oracle.forward(Q, K, V, m=m, k=17, s=2, causal=True, threads=1)
+    np.testing.assert_array_equal(a["I"], b["I"])
+    np.testing.assert_array_equal(a["E"], b["E"])
+    np.testing.assert_allclose(b["Vt"][0, m - 1], a["Vt"][0, m - 1], rtol=1e-14)
+    assert not np.allclose(b["Vt"][0, 0], a["Vt"][0, 0])
+
+
+def test_causal_rejects_2d_pooling():
+    Q = _rand((1, 64, 2), 90)
+    with pytest.raises(ValueError):
+        oracle.forward(Q, Q, Q, m=4, k=8, s=1, grid=(8, 8), lm=(2, 2), causal=True)
