@@ -292,10 +292,22 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time every configuration (vision, 32k, 131k and the m/k/s sweep) against its roofline, "
                          "one JSON line each, instead of the benchmark line")
+    ap.add_argument("--context", action="store_true",
+                    help="time dense softmax attention (torch scaled_dot_product_attention, bf16) beside the MiTA "
+                         "forward over N = 4k .. 128k at the long-context head shape, one JSON line per N")
+    ap.add_argument("--inference-mk", action="store_true",
+                    help="time the MiTA forward on one fixed input while m and k grow beyond the training values "
+                         "(the pages' inference-time knob), one JSON line per (m, k)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed steps
     if args.sweep:
         sweep(args)
+        return
+    if args.context:
+        context(args)
+        return
+    if args.inference_mk:
+        inference_mk(args)
         return
 
     from compressed_attention_adaptive_gb300 import synth
@@ -439,6 +451,92 @@ def pinned_host(nbytes, torch):
         return t, "mmap+MADV_HUGEPAGE+cudaHostRegister"
     except Exception:
         return torch.empty(nbytes, dtype=torch.uint8).pin_memory(), "torch pin_memory"
+
+
+def _time_cuda(fn, steps, warmup):
+    """Mean milliseconds of fn() over `steps` calls after `warmup`, CUDA events."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def context(args):
+    """Dense softmax attention against the MiTA forward over N at the
+    long-context head shape (B=1, H=16, d=128; MiTA m=128, k=256, s=2):
+    the measured counterpart of the pages' speed-up over standard attention.
+    The dense arm is PyTorch's scaled_dot_product_attention in bf16 (a library
+    flash-attention kernel), non-causal; inputs are the clustered synthetic
+    long-context draws. Neither arm is part of the other."""
+    import numpy as np
+    import torch
+    import torch.nn.functional as F
+    import compressed_attention_adaptive_gb300 as mita
+    from compressed_attention_adaptive_gb300 import synth
+    dev = torch.device("cuda", 0)
+    base = synth.WORKLOADS["longctx_n32k"]
+    for N in (4096, 8192, 16384, 32768, 65536, 131072):
+        w = base.with_(B=1, H=16, N=N)
+        Qn, Kn, Vn = synth.make_inputs(w, seed=0)
+        tt = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        Q, K, V = tt(Qn), tt(Kn), tt(Vn)
+        O = torch.empty_like(Q)
+        p = mita.params_for(Q, w.m, w.k, w.s)
+        ws = mita.workspace(p, dev)
+        steps = max(3, min(args.steps, 20 if N <= 32768 else 5))
+        t_mita = _time_cuda(lambda: mita.mita_forward(p, Q, K, V, O, ws), steps, args.warmup)
+        mita.mita_device_status(ws)
+        t_sdpa = _time_cuda(lambda: F.scaled_dot_product_attention(Q, K, V), steps, args.warmup)
+        print(json.dumps({"N": N, "B": w.B, "H": w.H, "d": w.d, "m": w.m, "k": w.k, "s": w.s, "dtype": "bf16",
+                          "mita_ms": t_mita, "sdpa_ms": t_sdpa, "speedup": t_sdpa / t_mita,
+                          "dense_flops": 4.0 * w.BH * N * N * w.d,
+                          "mita_flops": 4.0 * w.BH * N * w.d * (2 * w.m + w.s * w.k)}), flush=True)
+        del Q, K, V, O, ws
+        torch.cuda.empty_cache()
+
+
+def inference_mk(args):
+    """One fixed input (the long-context draw at B=1, H=16, N=32768), the
+    MiTA forward with m and k raised beyond the training values (m=128,
+    k=256): time per forward, the roofline of each point, and the change of
+    the output against the training setting (relative Frobenius distance)."""
+    import numpy as np
+    import torch
+    import compressed_attention_adaptive_gb300 as mita
+    from compressed_attention_adaptive_gb300 import synth
+    dev = torch.device("cuda", 0)
+    pk, pk_src = peaks()
+    w0 = synth.WORKLOADS["longctx_n32k"].with_(B=1, H=16)
+    Qn, Kn, Vn = synth.make_inputs(w0, seed=0)
+    tt = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    Q, K, V = tt(Qn), tt(Kn), tt(Vn)
+    ref = None
+    for m, k in ((128, 256), (128, 512), (128, 1024), (256, 256), (256, 512), (256, 1024), (512, 512),
+                 (512, 1024), (512, 2048)):
+        w = w0.with_(m=m, k=k)
+        O = torch.empty_like(Q)
+        p = mita.params_for(Q, m, k, w.s)
+        ws = mita.workspace(p, dev)
+        ms = _time_cuda(lambda: mita.mita_forward(p, Q, K, V, O, ws), max(3, min(args.steps, 20)), args.warmup)
+        mita.mita_device_status(ws)
+        Of = O.float()
+        if ref is None:
+            ref = Of.clone()
+        F_, B_ = work_counts(w)
+        t_roof = max(F_ / (pk["bf16_tflops"] * 1e12), B_ / (pk["hbm_gbs"] * 1e9))
+        print(json.dumps({"m": m, "k": k, "s": w.s, "N": w.N, "B": w.B, "H": w.H, "d": w.d, "ms": ms,
+                          "value": w.BH * w.N / (ms * 1e-3), "unit": UNIT, "t_roof_us": t_roof * 1e6,
+                          "frac": t_roof / (ms * 1e-3),
+                          "rel_change_vs_m128_k256": float((Of - ref).norm() / ref.norm())}), flush=True)
+        del O, ws
+        torch.cuda.empty_cache()
 
 
 def e2e_run(mita, p, Qn, Kn, Vn, w, dev, steps, dist, world):

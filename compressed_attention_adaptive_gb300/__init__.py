@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libmita.so")
 _lib = None
 
 F32, BF16 = 0, 1
-FLAG_NO_SHARED, FLAG_SIMT = 1, 2
+FLAG_NO_SHARED, FLAG_SIMT, FLAG_CAUSAL = 1, 2, 4
 TESTFLAG_STALL_PRODUCER = 1 << 31  # fault test only (see include/mita.h)
 STATUS = {0: "MITA_OK", 1: "MITA_ERR_INVALID_ARG", 2: "MITA_ERR_UNSUPPORTED", 3: "MITA_ERR_WORKSPACE",
           4: "MITA_ERR_CUDA", 5: "MITA_ERR_TIMEOUT", 6: "MITA_ERR_BOUNDS"}

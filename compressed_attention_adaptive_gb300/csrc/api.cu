@@ -67,8 +67,10 @@ static mita_status resolve(const mita_params* p, Dims* D) {
     if (p->s < 1 || p->s > p->m) return fail(MITA_ERR_INVALID_ARG, "s must be in [1, m]");
     if (p->s > kMaxS) return fail(MITA_ERR_UNSUPPORTED, "s > %d is not supported", kMaxS);
     if (p->dtype != MITA_DTYPE_F32 && p->dtype != MITA_DTYPE_BF16) return fail(MITA_ERR_INVALID_ARG, "bad dtype");
-    if (p->flags & ~(unsigned)(MITA_FLAG_NO_SHARED | MITA_FLAG_SIMT | MITA_TESTFLAG_STALL_PRODUCER))
+    if (p->flags & ~(unsigned)(MITA_FLAG_NO_SHARED | MITA_FLAG_SIMT | MITA_FLAG_CAUSAL | MITA_TESTFLAG_STALL_PRODUCER))
         return fail(MITA_ERR_INVALID_ARG, "unknown flag");
+    if ((p->flags & MITA_FLAG_CAUSAL) && p->grid_h != 0)
+        return fail(MITA_ERR_INVALID_ARG, "the causal variant needs 1-D pooling (grid_h == 0)");
     if (!(p->scale >= 0.0f) || isinf(p->scale)) return fail(MITA_ERR_INVALID_ARG, "scale must be finite and >= 0");
     if ((long long)p->B * p->H > 65535) return fail(MITA_ERR_UNSUPPORTED, "B*H must be <= 65535");
     if ((long long)p->B * p->H * p->N >= (1LL << 31)) return fail(MITA_ERR_UNSUPPORTED, "B*H*N must be < 2^31");
@@ -89,6 +91,11 @@ static mita_status resolve(const mita_params* p, Dims* D) {
     D->flags = p->flags;
     D->dtype = p->dtype;
     D->shared = !(p->flags & MITA_FLAG_NO_SHARED);
+    D->causal = (p->flags & MITA_FLAG_CAUSAL) != 0;
+    if (D->causal && !(p->flags & MITA_FLAG_SIMT) && tc_supported(*D) && !tc_plan(*D).resident)
+        return fail(MITA_ERR_UNSUPPORTED,
+                    "the causal variant runs on the tensor-core path only for m <= 128, k <= 256 with the shared "
+                    "slots on (MITA_FLAG_SIMT runs it on CUDA cores)");
     if (out_simt_smem(*D) > 200 * 1024) return fail(MITA_ERR_UNSUPPORTED, "m + s*k too large for this library");
     return MITA_OK;
 }

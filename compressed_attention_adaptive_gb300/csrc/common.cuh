@@ -23,6 +23,7 @@ struct Dims {
     unsigned flags;
     int dtype;         // 0 f32, 1 bf16
     bool shared;       // shared slots present
+    bool causal;       // causal variant (1-D pooling only)
 };
 
 __device__ __forceinline__ float to_f(float x) { return x; }
@@ -93,6 +94,13 @@ __device__ __forceinline__ int block_excl_scan(int v, int* tmp, int* total) {
     __syncthreads();
     *total = tmp[nw];
     return tmp[w] + x - v;
+}
+
+// Causal variant (1-D pooling): landmark i's bin is complete for query t once
+// its end hi_i = ceil((i + 1) N / m) <= t + 1; the number of such landmarks.
+__host__ __device__ __forceinline__ int landmarks_complete(int t, int N, int m) {
+    // largest i + 1 with (i + 1) N <= (t + 1) m, i.e. floor((t + 1) m / N)
+    return (int)(((long long)(t + 1) * m) / N);
 }
 
 // Adaptive-average-pooling bin [lo, hi) of bin i when L cells pool to P bins.

@@ -150,16 +150,19 @@ __global__ void __launch_bounds__(256) k_gemm_nt(const TA* __restrict__ A, long 
 // --------------------------------------------------------- shared expert
 
 // Per landmark row of raw scores S (length N): stats = (max of scale*s,
-// 1 / sum exp(scale*s - max)).
-__global__ void __launch_bounds__(256) k_row_softmax_stats(const float* __restrict__ S, int N, float scale,
-                                                           float2* __restrict__ stats) {
+// 1 / sum exp(scale*s - max)); over the keys of the landmark's prefix
+// j < hi_i only in the causal variant.
+__global__ void __launch_bounds__(256) k_row_softmax_stats(const float* __restrict__ S, int N, int m, int causal,
+                                                           float scale, float2* __restrict__ stats) {
     __shared__ float red[32];
     const float* s = S + (size_t)blockIdx.x * N;
+    int lo, hi = N;
+    if (causal) pool_bin(blockIdx.x % m, N, m, &lo, &hi);
     float mx = -INFINITY;
-    for (int j = threadIdx.x; j < N; j += blockDim.x) mx = fmaxf(mx, scale * s[j]);
+    for (int j = threadIdx.x; j < hi; j += blockDim.x) mx = fmaxf(mx, scale * s[j]);
     mx = block_max(mx, red);
     float sum = 0.0f;
-    for (int j = threadIdx.x; j < N; j += blockDim.x) sum += expf(scale * s[j] - mx);
+    for (int j = threadIdx.x; j < hi; j += blockDim.x) sum += expf(scale * s[j] - mx);
     sum = block_sum(sum, red);
     if (threadIdx.x == 0) stats[blockIdx.x] = make_float2(mx, 1.0f / sum);
 }
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(256) k_row_softmax_stats(const float* __restri
 template <typename T>
 __global__ void __launch_bounds__(256) k_pv_simt(const float* __restrict__ S, const float2* __restrict__ stats,
                                                  const T* __restrict__ V, float* __restrict__ Vt, int m, int N,
-                                                 int d, float scale) {
+                                                 int d, float scale, int causal) {
     __shared__ __align__(16) float As[16][68];
     __shared__ __align__(16) float Bs[16][68];
     const int b = blockIdx.z, m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
@@ -185,7 +188,9 @@ __global__ void __launch_bounds__(256) k_pv_simt(const float* __restrict__ S, co
             {
                 const int row = e >> 4, kk = e & 15, gi = m0 + row, gk = k0 + kk;
                 float p = 0.0f;
-                if (gi < m && gk < N) {
+                int lo, hi = N;
+                if (causal && gi < m) pool_bin(gi, N, m, &lo, &hi);
+                if (gi < m && gk < hi) {
                     const float2 sx = st[gi];
                     p = expf(scale * Sb[(size_t)gi * N + gk] - sx.x) * sx.y;
                 }
@@ -263,6 +268,9 @@ __global__ void __launch_bounds__(128) k_out_simt(const T* __restrict__ Q, const
     int* src = reinterpret_cast<int*>(lg + nslot);
     const long long qg = blockIdx.x;
     const int bh = (int)(qg / D.N);
+    const int tq = (int)(qg % D.N);  // the query's position
+    // causal variant: the shared slots of complete bins, routed keys up to tq
+    const int m_ok = D.causal ? landmarks_complete(tq, D.N, D.m) : D.m;
     const T* Kb = K + (size_t)bh * D.N * d;
     const T* Vb = V + (size_t)bh * D.N * d;
     const float* Qtb = Qt + (size_t)bh * D.m * d;
@@ -274,6 +282,11 @@ __global__ void __launch_bounds__(128) k_out_simt(const T* __restrict__ Q, const
         float dot = 0.0f;
         int j;
         if (u < m_sh) {
+            if (u >= m_ok) {
+                src[u] = INT_MIN;
+                lg[u] = -INFINITY;
+                continue;
+            }
             j = -1 - u;
             const float* kr = Qtb + (size_t)u * d;
             for (int c = 0; c < d; ++c) dot = fmaf(qv[c], kr[c], dot);
@@ -283,6 +296,11 @@ __global__ void __launch_bounds__(128) k_out_simt(const T* __restrict__ Q, const
             j = (e >= 0 && e < D.m) ? I[((size_t)bh * D.m + e) * D.k + t] : -1;
             if (e < 0 || e >= D.m || j < 0 || j >= D.N) {
                 set_status(status, kStBounds);
+                src[u] = INT_MIN;
+                lg[u] = -INFINITY;
+                continue;
+            }
+            if (D.causal && j > tq) {
                 src[u] = INT_MIN;
                 lg[u] = -INFINITY;
                 continue;
@@ -302,7 +320,7 @@ __global__ void __launch_bounds__(128) k_out_simt(const T* __restrict__ Q, const
         sum += p;
     }
     sum = block_sum(sum, red);
-    const float inv = 1.0f / sum;
+    const float inv = sum > 0.0f ? 1.0f / sum : 0.0f;  // no slot (causal only): a zero row
     for (int c = threadIdx.x; c < d; c += blockDim.x) {
         float acc = 0.0f;
         for (int u = 0; u < nslot; ++u) {
@@ -365,9 +383,9 @@ cudaError_t launch_select_simt(const Dims& D, const void* Q, const void* K, cons
 template <typename T>
 static cudaError_t shared_simt_t(const Dims& D, const void* V, const float* S, float2* stats, float* Vt,
                                  cudaStream_t st) {
-    k_row_softmax_stats<<<D.BH * D.m, 256, 0, st>>>(S, D.N, D.scale, stats);
+    k_row_softmax_stats<<<D.BH * D.m, 256, 0, st>>>(S, D.N, D.m, D.causal ? 1 : 0, D.scale, stats);
     dim3 grid((D.d + 63) / 64, (D.m + 63) / 64, D.BH);
-    k_pv_simt<T><<<grid, 256, 0, st>>>(S, stats, (const T*)V, Vt, D.m, D.N, D.d, D.scale);
+    k_pv_simt<T><<<grid, 256, 0, st>>>(S, stats, (const T*)V, Vt, D.m, D.N, D.d, D.scale, D.causal ? 1 : 0);
     count_launch(2);
     return cudaGetLastError();
 }

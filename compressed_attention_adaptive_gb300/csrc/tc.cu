@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(320, 1)
                   const __nv_bfloat16* __restrict__ Qhi, const __nv_bfloat16* __restrict__ Qlo,
                   const float* __restrict__ thr, int2* __restrict__ cand, int* __restrict__ ccount,
                   float* __restrict__ Opart, float2* __restrict__ ML, int N, int m, int m_pad, int splits,
-                  int chunks_per_split, float sl, int stall, int* __restrict__ status) {
+                  int chunks_per_split, float sl, int causal, int stall, int* __restrict__ status) {
     constexpr int TILE = kT * D * 2;
     constexpr int DH = D / 2;
     constexpr uint32_t kS0 = 0, kO = 256;
@@ -445,6 +445,10 @@ __global__ void __launch_bounds__(320, 1)
         const int row = mt * kT + r;
         const bool row_ok = row < m;
         const float th = row_ok ? thr[(size_t)bh * m + row] : 0.0f;
+        // causal variant: the shared expert of landmark `row` attends to the keys
+        // of its prefix, j < hi (the top-k candidates still come from every key)
+        int lo_row, hi_row = N;
+        if (causal && row_ok) pool_bin(row, N, m, &lo_row, &hi_row);
         const long long capw = (long long)chunks_per_split * 64;
         const size_t region = (((size_t)bh * m_pad + row) * splits + sp) * 2 + wg;
         int2* cw = cand + region * capw;
@@ -457,13 +461,14 @@ __global__ void __launch_bounds__(320, 1)
             if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (c >> 1) & 1, status, abort_v, lim))) { ok = false; break; }
             fence_after_sync();
             const uint32_t tS = lane_base(tmem) + kS0 + sb * 128;
-            const int nval = row_ok ? min(kT, j_end - j0) - 64 * wg : 0;
+            const int nval = row_ok ? min(kT, j_end - j0) - 64 * wg : 0;   // real keys of this half
+            const int nsm = min(nval, hi_row - j0 - 64 * wg);               // ... inside the softmax
             float v[64];
             tmem_ld32(tS + 64 * wg, v);
             tmem_ld32(tS + 64 * wg + 32, v + 32);
             tmem_wait_ld();
             float mx = -INFINITY;
-            if (nval >= 64 && sl > 0.0f) {  // every column real: one tree maximum
+            if (nsm >= 64 && sl > 0.0f) {  // every column real: one tree maximum
 #pragma unroll
                 for (int j = 0; j < 64; ++j) emit_cand(cw, ncand, v[j], j0 + 64 * wg + j, v[j] >= th);
                 mx = max64(v) * sl;
@@ -471,7 +476,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
                     emit_cand(cw, ncand, v[j], j0 + 64 * wg + j, j < nval && v[j] >= th);
-                    mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
+                    mx = fmaxf(mx, j < nsm ? v[j] * sl : -INFINITY);
                 }
             }
             xmax[c & 1][wg][r] = mx;
@@ -491,7 +496,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int j = 0; j < 64; j += 2) {
                 const float e0 = ex2(fmaf(v[j], sl, -mnew)), e1 = ex2(fmaf(v[j + 1], sl, -mnew));
-                const float p0 = j < nval ? e0 : 0.0f, p1 = j + 1 < nval ? e1 : 0.0f;
+                const float p0 = j < nsm ? e0 : 0.0f, p1 = j + 1 < nsm ? e1 : 0.0f;
                 sum += p0 + p1;
                 pkd[j >> 1] = pack_bf16(p0, p1);
             }
@@ -736,7 +741,7 @@ template <int D, int SMAX, int NSQ>
 __global__ void __launch_bounds__(320, 1)
     k_route_ws(const __grid_constant__ CUtensorMap tmQ, const __nv_bfloat16* __restrict__ Qhi,
                const __nv_bfloat16* __restrict__ Qlo, const __nv_bfloat16* __restrict__ Vtb, int N, int m, int s,
-               int tiles_per_head, int total_tiles, float sl, int32_t* __restrict__ E,
+               int tiles_per_head, int total_tiles, float sl, int causal, int32_t* __restrict__ E,
                __nv_bfloat16* __restrict__ sh_part, float* __restrict__ sh_lse, int* __restrict__ status) {
     constexpr int TILE = kT * D * 2;
     constexpr int DH = D / 2;
@@ -902,7 +907,7 @@ __global__ void __launch_bounds__(320, 1)
                 if (!__all_sync(0xffffffffu, ws_wait(&ebar, 0, status, abort_v))) return false;
                 lt = lsum + xl[pt & 1][wg ^ 1][r];
             }
-            const float inv = 1.0f / lt;
+            const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;  // no slot (causal only): zero partial
             const size_t row0 = (size_t)bh * N + q0 + (r & ~31);  // this warp's first row
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // lanes 16h .. 16h + 15 stage their rows
@@ -925,7 +930,7 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 __syncwarp();
             }
-            if (wg == 0 && q < N) sh_lse[(size_t)bh * N + q] = mx + __log2f(lt);
+            if (wg == 0 && q < N) sh_lse[(size_t)bh * N + q] = lt > 0.0f ? mx + __log2f(lt) : -INFINITY;
             return true;
         };
         bool ok = true;
@@ -938,6 +943,10 @@ __global__ void __launch_bounds__(320, 1)
             fence_after_sync();
             const uint32_t tR = lane_base(tmem) + kR0 + rb * 128;
             const int nval = min(64, m - 64 * wg);  // landmarks of this half
+            // causal variant: the shared slots are the landmarks whose bin is
+            // complete at query q (a prefix of the landmarks); routing still
+            // ranks all of them
+            const int nsm = causal ? min(nval, landmarks_complete(q_ok ? q : N - 1, N, m) - 64 * wg) : nval;
             float v[64];
             tmem_ld32(tR + 64 * wg, v);
             tmem_ld32(tR + 64 * wg + 32, v + 32);
@@ -947,10 +956,10 @@ __global__ void __launch_bounds__(320, 1)
             for (int j = 0; j < 64; ++j) v[j] = j < nval ? v[j] : -INFINITY;
             const float hmax = max64(v);  // largest raw score of this half
             float mx = hmax * sl;
-            if (!(sl > 0.0f)) {  // a negative scale turns the smallest score into the largest logit
-                mx = -INFINITY;
+            if (!(sl > 0.0f) || nsm < nval) {  // a negative scale turns the smallest score into the largest
+                mx = -INFINITY;               // logit; a causal row has fewer slots
 #pragma unroll
-                for (int j = 0; j < 64; ++j) mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
+                for (int j = 0; j < 64; ++j) mx = fmaxf(mx, j < nsm ? v[j] * sl : -INFINITY);
             }
             xmax[tl & 1][wg][r] = mx;
             if (tl > 0) xl[(tl - 1) & 1][wg][r] = plsum;  // the previous tile's row-sum half
@@ -965,7 +974,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int j = 0; j < 64; j += 2) {
                 const float e0 = ex2(fmaf(v[j], sl, -mx)), e1 = ex2(fmaf(v[j + 1], sl, -mx));
-                const float p0 = j < nval ? e0 : 0.0f, p1 = j + 1 < nval ? e1 : 0.0f;
+                const float p0 = j < nsm ? e0 : 0.0f, p1 = j + 1 < nsm ? e1 : 0.0f;
                 lsum += p0 + p1;
                 pkd[j >> 1] = pack_bf16(p0, p1);
             }
@@ -1225,7 +1234,7 @@ __global__ void __launch_bounds__(256) k_merge(const __nv_bfloat16* __restrict__
 #pragma unroll
     for (int j = 0; j <= kMaxS; ++j) {
         if (j < kMaxS ? j >= s : !sh_part) continue;
-        const float w = exp2f(lj[j] - L);
+        const float w = lj[j] > -INFINITY ? exp2f(lj[j] - L) : 0.0f;  // an empty partial (causal only) weighs 0
         wsum += w;
         const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
 #pragma unroll
@@ -1235,7 +1244,7 @@ __global__ void __launch_bounds__(256) k_merge(const __nv_bfloat16* __restrict__
             acc[2 * v + 1] = fmaf(w, f.y, acc[2 * v + 1]);
         }
     }
-    const float winv = 1.0f / wsum;
+    const float winv = wsum > 0.0f ? 1.0f / wsum : 0.0f;  // no slot at all (causal only): a zero row
     *reinterpret_cast<uint4*>(O + qi * D + gcol) =
         make_uint4(pack_bf16(acc[0] * winv, acc[1] * winv), pack_bf16(acc[2] * winv, acc[3] * winv),
                    pack_bf16(acc[4] * winv, acc[5] * winv), pack_bf16(acc[6] * winv, acc[7] * winv));
@@ -1678,7 +1687,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                  const __nv_bfloat16* __restrict__ V, const int32_t* __restrict__ I, const int32_t* __restrict__ perm,
                  const int4* __restrict__ tiles, const int2* __restrict__ xtl, int nx, int* __restrict__ work_ctr,
                  __nv_bfloat16* __restrict__ part, float* __restrict__ lse, int N, int m, int k, int s, float sl,
-                 int stall, int* __restrict__ status) {
+                 int causal, int stall, int* __restrict__ status) {
     constexpr int TILE = kT * D * 2;
     constexpr uint32_t kS0 = 0, kO0 = 256;  // TMEM: S/P buffers 0 / 128, O buffers 256 / 384
     extern __shared__ uint8_t smem_raw[];
@@ -1694,7 +1703,9 @@ __global__ void __launch_bounds__(kResThreads, 1)
     __shared__ int4 pnext[2];    // producer warp 0 -> all producer warps: the tile to load (w < 0: none)
     __shared__ int pstop;        // producer warp 0 -> all producer warps: stop (a wait failed)
     __shared__ int rowq[2][kT];  // q << 3 | slot of each tile row, -1 past the tile's rows
+    __shared__ int rowok[2][kT]; // causal variant: keys of the row's expert at or before its query
     __shared__ int keyrow[kT];
+    __shared__ int keyall[2 * kT];  // causal variant: the current expert's key indices (ascending)
     __shared__ float xmax[2][2][kT], xl[2][2][kT];  // [parity][half][row] exchange of the two softmax halves
     __shared__ uint64_t xbar[2], ebar[2];          // exchange barriers (per chunk / per tile), one arrival per warp
     __shared__ uint32_t tmem_slot;
@@ -1813,6 +1824,35 @@ __global__ void __launch_bounds__(kResThreads, 1)
                     pk = -1;
                 }
                 rowq[qs][r] = r < rows ? pk : -1;
+            }
+            if (causal) {
+                // each row's count of expert keys at or before its query: the
+                // expert's indices are ascending, so a binary search per row
+                if (reload) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int i = 0; i < kT / 32; ++i)
+                            if (own(lane + 32 * i) && c * kT + lane + 32 * i < k)
+                                keyall[c * kT + lane + 32 * i] = krv[c][i];
+                    named_sync(1, 32 * kNPW);
+                }
+#pragma unroll
+                for (int i = 0; i < kT / 32; ++i) {
+                    const int r = lane + 32 * i;
+                    if (!own(r)) continue;
+                    const int pk = rowq[qs][r];
+                    int lo = 0, hi = k;  // first index with key > q
+                    if (pk >= 0) {
+                        const int q = pk >> 3;
+                        while (lo < hi) {
+                            const int mid = (lo + hi) >> 1;
+                            if (keyall[mid] <= q) lo = mid + 1;
+                            else hi = mid;
+                        }
+                    }
+                    rowok[qs][r] = lo;
+                }
             }
             if (pw == 0 && lane == 0) tinfo[qs] = ResTile{bh, e, start, rows, gen + (reload ? 1 : 0)};
             __syncwarp();
@@ -2016,7 +2056,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 __syncwarp();
             }
             if (lane == 0) mbar_arrive(&o_free[ob]);
-            const float inv = pk >= 0 ? 1.0f / lt : 0.0f;
+            const float inv = (pk >= 0 && lt > 0.0f) ? 1.0f / lt : 0.0f;  // no key (causal only): zero partial
             const size_t pr = pk >= 0 ? ((size_t)pti.bh * N + (pk >> 3)) * s + (pk & 7) : 0;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // lanes 16h .. 16h + 15 stage their rows
@@ -2040,7 +2080,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 }
                 __syncwarp();
             }
-            if (wg == 0 && pk >= 0) lse[pr] = pm + __log2f(lt);
+            if (wg == 0 && pk >= 0) lse[pr] = lt > 0.0f ? pm + __log2f(lt) : -INFINITY;
             return true;
         };
         int g = 0;
@@ -2058,6 +2098,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
             const ResTile ti = tinfo[qs];
             if (ti.rows < 0) break;  // end of the work
             const int pk = rowq[qs][r];
+            const int kok = causal ? rowok[qs][r] : k;  // the row's keys (a prefix of the expert's)
             __syncwarp();
             if (lane == 0) mbar_arrive(&q_empty[qs]);  // tinfo / rowq read; the MMA releases the tile itself
             const bool valid = pk >= 0;
@@ -2068,7 +2109,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (g >> 1) & 1, status, abort_v, lim))) { ok = false; break; }
                 fence_after_sync();
                 const uint32_t tS = lane_base(tmem) + kS0 + sb * 128;
-                const int nval = valid ? min(kT, k - c * kT) - 64 * wg : 0;  // valid columns of this half
+                const int nval = valid ? min(kT, kok - c * kT) - 64 * wg : 0;  // valid columns of this half
                 const bool full = __all_sync(0xffffffffu, nval >= 64) && fast;
                 float v[64];
                 tmem_ld32(tS + 64 * wg, v);
@@ -2266,8 +2307,8 @@ static cudaError_t launch_route_s(const Dims& D, const TcPlan& P, const TcWork& 
         const int total = tph * D.BH;
         const int grid = std::min(total, num_sms());
         k_route_ws<DD, SMAX, NSQ><<<grid, 320, smem, st>>>(mq, W.Qhi, W.Qlo, W.Vtb, D.N, D.m, D.s, tph, total,
-                                                           D.scale * 1.4426950408889634f, E, W.sh_part, W.sh_lse,
-                                                           status);
+                                                           D.scale * 1.4426950408889634f, D.causal ? 1 : 0, E,
+                                                           W.sh_part, W.sh_lse, status);
     } else if (P.m_pad <= 256) {
         const int smem = 2 * P.m_pad * DD * 2 + 2 * tile + 1024;
         if ((e = set_smem(k_route_tc<DD, SMAX>, smem))) return e;
@@ -2335,6 +2376,7 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
         dim3 grid(P.m_tiles, P.splits, D.BH);
         k_landmark_ws<DD, NS><<<grid, 320, smem, st>>>(mk, mv, W.Qhi, W.Qlo, W.thr, W.cand, W.ccount, W.Opart, W.ML,
                                                       D.N, D.m, P.m_pad, P.splits, P.chunks_per_split, sl,
+                                                      D.causal ? 1 : 0,
                                                       (D.flags & MITA_TESTFLAG_STALL_PRODUCER) ? 1 : 0, status);
         if ((e = cudaGetLastError())) return e;
         count_launch();
@@ -2377,7 +2419,7 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
             if ((e = set_smem(k_expert_res<DD>, smem))) return e;
             k_expert_res<DD><<<num_sms(), kResThreads, smem, st>>>(
                 q, kk, v, I, W.perm, W.tiles, W.xtl, D.BH * D.m, W.tile_ctr + 1, W.part, W.lse, D.N, D.m, D.k, D.s,
-                sl, (D.flags & MITA_TESTFLAG_STALL_PRODUCER) ? 1 : 0, status);
+                sl, D.causal ? 1 : 0, (D.flags & MITA_TESTFLAG_STALL_PRODUCER) ? 1 : 0, status);
             if ((e = cudaGetLastError())) return e;
             count_launch();
             prof_mark(st, "merge");

@@ -69,7 +69,19 @@ enum {
     MITA_FLAG_NO_SHARED = 1u << 0,
     /* Run every step on CUDA cores in fp32 even where the tensor-core path
      * applies (a second GPU implementation for cross-checks). */
-    MITA_FLAG_SIMT = 1u << 1
+    MITA_FLAG_SIMT = 1u << 1,
+    /* The causal variant (the summaries describe none; these rules are this
+     * library's reading, for 1-D pooling only): the shared expert of landmark
+     * i attends to the keys of its prefix, j < hi_i, where [lo_i, hi_i) is
+     * its pooling bin; query t has landmark i's shared slot only once that bin
+     * is complete (hi_i <= t + 1); expert sets and routes are selected as in
+     * the non-causal pass, and of a routed expert's keys query t attends to
+     * those with j <= t; a query left with no slot gets a zero output row.
+     * Runs on the tensor-core path when m <= 128, k <= 256 and the shared
+     * slots are on, and on the CUDA-core path (float32, or MITA_FLAG_SIMT);
+     * other shapes return MITA_ERR_UNSUPPORTED. With 2-D pooling it is
+     * MITA_ERR_INVALID_ARG. */
+    MITA_FLAG_CAUSAL = 1u << 2
 };
 
 /* Fault test of the device-side failure detection, not for production: in

@@ -109,7 +109,7 @@ def run_gpu(w, Qn, Kn, Vn, flags=0, scale=0.0):
 
 
 def oracle_parallel(Q, K, V, w, q_ids=None, I_override=None, E_override=None, no_shared=False, scale=0.0,
-                    chunks=None):
+                    chunks=None, causal=False):
     """oracle.forward over heads Q, K, V [H, N, d], with each head's queries
     split into chunks that run on separate host threads (each chunk repeats the
     head's landmark pass; the oracle itself is unchanged). Returns the same
@@ -128,7 +128,7 @@ def oracle_parallel(Q, K, V, w, q_ids=None, I_override=None, E_override=None, no
         Eo = None if E_override is None else E_override[h:h + 1, p]
         return oracle.forward(Q[h:h + 1], K[h:h + 1], V[h:h + 1], w.m, w.k, w.s, grid=w.grid, lm=w.lm,
                               scale=scale, no_shared=no_shared, q_ids=qs[p], I_override=Io, E_override=Eo,
-                              threads=1)
+                              threads=1, causal=causal)
 
     with ThreadPoolExecutor(min(cores, len(jobs))) as ex:
         res = list(ex.map(one, jobs))
@@ -143,7 +143,7 @@ def oracle_parallel(Q, K, V, w, q_ids=None, I_override=None, E_override=None, no
     return out
 
 
-def check_heads(w, Qn, Kn, Vn, g, heads, q_ids=None, no_shared=False, scale=0.0, label=None):
+def check_heads(w, Qn, Kn, Vn, g, heads, q_ids=None, no_shared=False, scale=0.0, label=None, causal=False):
     """Checks heads (flat ids) of the GPU result g against the oracle."""
     BH = w.B * w.H
     flat = lambda a: a.reshape((BH,) + a.shape[2:])
@@ -152,7 +152,8 @@ def check_heads(w, Qn, Kn, Vn, g, heads, q_ids=None, no_shared=False, scale=0.0,
     gI, gE, gO, gVt, gQt = (flat(g[x])[heads] for x in ("I", "E", "O", "Vt", "Qt"))
     if q_ids is not None:
         gE, gO = gE[:, q_ids], gO[:, q_ids]
-    ref = oracle_parallel(Q, K, V, w, q_ids=q_ids, I_override=gI, E_override=gE, no_shared=no_shared, scale=scale)
+    ref = oracle_parallel(Q, K, V, w, q_ids=q_ids, I_override=gI, E_override=gE, no_shared=no_shared, scale=scale,
+                          causal=causal)
     rtol_qt = 1e-5 if w.dtype == "bf16" else 1e-6
     np.testing.assert_allclose(gQt, ref["Qt"], rtol=rtol_qt, atol=1e-6)
     stats = {"exact": 0, "tol": 0}

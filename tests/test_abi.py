@@ -73,3 +73,12 @@ def test_flag_values_match_the_header(lib):
     assert mita.TESTFLAG_STALL_PRODUCER == 1 << 31
     # the fault-test flag is a valid flag (accepted on the host, like the others)
     assert mita.mita_workspace_size(_p(flags=mita.TESTFLAG_STALL_PRODUCER)) > 0
+
+
+def test_causal_flag_validation(lib):
+    C = mita.FLAG_CAUSAL
+    assert mita.mita_workspace_size(_p(flags=C)) > 0                                      # resident shape
+    assert mita.mita_workspace_size(_p(flags=C, grid_h=32, grid_w=32, lm_h=4, lm_w=4)) == 0  # 2-D pooling
+    assert mita.mita_workspace_size(_p(flags=C, k=512)) == 0                              # unsupported on tcgen05
+    assert mita.mita_workspace_size(_p(flags=C | mita.FLAG_SIMT, k=512)) > 0               # CUDA cores run it
+    assert mita.mita_workspace_size(_p(flags=C, dtype=mita.F32, k=512)) > 0

@@ -131,3 +131,14 @@ def test_full_n131k():
 @pytest.mark.parametrize("name", [w.name for w in synth.sweep_workloads()])
 def test_full_sweep_points(name):
     _full(synth.get(name), heads=[7], n_q=1024)
+
+
+# ---------------------------------------------- m and k raised at inference
+# The pages note that m and k can be raised at inference time without
+# retraining (Dutch edition, "Algorithmische Generalisatie"): the same fixed
+# input as the benchmark's inference sweep, at the largest settings it times.
+
+@pytest.mark.slow
+@pytest.mark.parametrize("m,k", [(256, 1024), (512, 2048)])
+def test_inference_raised_m_k(m, k):
+    _full(L["longctx_n32k"].with_(B=1, H=16, m=m, k=k), heads=[5], n_q=1024)
