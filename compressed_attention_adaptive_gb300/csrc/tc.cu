@@ -1876,7 +1876,9 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 const __nv_bfloat16* Kb = K + (size_t)bh * N * D;
                 const __nv_bfloat16* Vb = V + (size_t)bh * N * D;
                 bool okc = true;
-                for (int c = 0; c < nex; ++c) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {  // nex <= 2 chunks (unrolled: krv stays in registers)
+                    if (c >= nex) break;
                     // every MMA on the previous keys of this chunk is done: the MMA
                     // warp commits kv_rel[c] once per change of keys (gen - 1 so far)
                     if (gen > 0) {
