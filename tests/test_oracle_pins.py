@@ -359,3 +359,66 @@ def test_causal_rejects_2d_pooling():
     Q = _rand((1, 64, 2), 90)
     with pytest.raises(ValueError):
         oracle.forward(Q, Q, Q, m=4, k=8, s=1, grid=(8, 8), lm=(2, 2), causal=True)
+
+
+# ------------------------------------------------------------- backward
+# The pages print no backward pass; oracle/backward.py is the chain rule with
+# the expert sets and routes held fixed. It is pinned against central finite
+# differences of the C forward oracle (run with the same sets and routes as
+# overrides) and, in the special case that reduces to softmax attention,
+# against PyTorch's autograd through scaled_dot_product_attention.
+
+from oracle import backward as obwd
+
+
+def _loss_fd(Q, K, V, dO, m, k, s, I, E, dirs, h=1e-5, no_shared=False):
+    """Central difference of L = sum(O * dO) along the direction dirs."""
+    def L(a):
+        Qp, Kp, Vp = (x + a * dx for x, dx in zip((Q, K, V), dirs))
+        O = oracle.forward(Qp, Kp, Vp, m, k, s, I_override=I, E_override=E, threads=1, no_shared=no_shared)["O"]
+        return float(np.sum(O * dO))
+    return (L(h) - L(-h)) / (2 * h)
+
+
+@pytest.mark.parametrize("N,d,m,k,s,no_shared", [(48, 6, 4, 7, 2, False), (40, 5, 5, 40, 1, False),
+                                                  (36, 4, 3, 9, 3, True), (30, 3, 7, 5, 2, False)])
+def test_backward_matches_finite_differences(N, d, m, k, s, no_shared):
+    rng = np.random.default_rng(100 + N)
+    Q, K, V, dO = (rng.standard_normal((1, N, d)) for _ in range(4))
+    r = oracle.forward(Q, K, V, m, k, s, threads=1, no_shared=no_shared)
+    dQ, dK, dV = obwd.backward(Q, K, V, dO, r["I"], r["E"], no_shared=no_shared)
+    for trial in range(3):
+        dirs = [rng.standard_normal((1, N, d)) for _ in range(3)]
+        fd = _loss_fd(Q, K, V, dO, m, k, s, r["I"], r["E"], dirs, no_shared=no_shared)
+        an = float(np.sum(dQ * dirs[0]) + np.sum(dK * dirs[1]) + np.sum(dV * dirs[2]))
+        assert abs(fd - an) <= 1e-7 * (1 + abs(fd)), (trial, fd, an)
+
+
+def test_backward_each_input_alone():
+    # the same check with one input perturbed at a time, so that a slip in one
+    # of dQ, dK, dV cannot hide behind the others
+    rng = np.random.default_rng(7)
+    N, d, m, k, s = 32, 4, 4, 6, 2
+    Q, K, V, dO = (rng.standard_normal((1, N, d)) for _ in range(4))
+    r = oracle.forward(Q, K, V, m, k, s, threads=1)
+    grads = obwd.backward(Q, K, V, dO, r["I"], r["E"])
+    for which in range(3):
+        dirs = [np.zeros((1, N, d)) for _ in range(3)]
+        dirs[which] = rng.standard_normal((1, N, d))
+        fd = _loss_fd(Q, K, V, dO, m, k, s, r["I"], r["E"], dirs)
+        an = float(np.sum(grads[which] * dirs[which]))
+        assert abs(fd - an) <= 1e-7 * (1 + abs(fd)), (which, fd, an)
+
+
+def test_backward_no_shared_full_k_is_attention_backward():
+    # shared slots off, k = N, s = 1: softmax attention, whose gradient
+    # PyTorch's autograd gives through scaled_dot_product_attention
+    rng = np.random.default_rng(8)
+    N, d = 24, 5
+    Q, K, V, dO = (rng.standard_normal((1, N, d)) for _ in range(4))
+    r = oracle.forward(Q, K, V, 3, N, 1, threads=1, no_shared=True)
+    dQ, dK, dV = obwd.backward(Q, K, V, dO, r["I"], r["E"], no_shared=True)
+    tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (Q, K, V))
+    torch.nn.functional.scaled_dot_product_attention(tq, tk, tv).backward(torch.from_numpy(dO))
+    for got, ref in ((dQ, tq.grad), (dK, tk.grad), (dV, tv.grad)):
+        np.testing.assert_allclose(got, ref.numpy(), rtol=1e-10, atol=1e-12)
