@@ -296,6 +296,8 @@ def main():
     ap.add_argument("--context", action="store_true",
                     help="time dense softmax attention (torch scaled_dot_product_attention, bf16) beside the MiTA "
                          "forward over N = 4k .. 128k at the long-context head shape, one JSON line per N")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (CUDA cores, fp32) on the long-context head shape at B=1, H=2")
     ap.add_argument("--inference-mk", action="store_true",
                     help="time the MiTA forward on one fixed input while m and k grow beyond the training values "
                          "(the pages' inference-time knob), one JSON line per (m, k)")
@@ -309,6 +311,9 @@ def main():
         return
     if args.inference_mk:
         inference_mk(args)
+        return
+    if args.backward:
+        backward_arm(args)
         return
 
     from compressed_attention_adaptive_gb300 import synth
@@ -538,6 +543,38 @@ def inference_mk(args):
                           "rel_change_vs_m128_k256": float((Of - ref).norm() / ref.norm())}), flush=True)
         del O, ws
         torch.cuda.empty_cache()
+
+
+def backward_arm(args):
+    """The backward pass (mita_backward, CUDA cores in fp32) on the long-context
+    head shape at B=1, H=2, N=32768, for the sets and routes of one forward
+    pass: time per call (CUDA events) and its arithmetic against the fp32 FMA
+    peak of the CUDA cores (152 SMs x 128 lanes x 2 flops x the SM clock)."""
+    import numpy as np
+    import torch
+    import compressed_attention_adaptive_gb300 as mita
+    from compressed_attention_adaptive_gb300 import synth
+    dev = torch.device("cuda", 0)
+    w = synth.WORKLOADS["longctx_n32k"].with_(B=1, H=2)
+    Qn, Kn, Vn = synth.make_inputs(w, seed=0)
+    tt = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    Q, K, V = tt(Qn), tt(Kn), tt(Vn)
+    dO = torch.randn_like(Q)
+    O, idx, route, _ = mita.forward(Q, K, V, w.m, w.k, w.s, return_sets=True)
+    p = mita.params_for(Q, w.m, w.k, w.s)
+    ws = torch.empty(mita.mita_backward_workspace_size(p), dtype=torch.uint8, device=dev)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    ms = _time_cuda(lambda: mita.mita_backward(p, Q, K, V, dO, idx, route, dQ, dK, dV, ws),
+                    max(3, min(args.steps, 10)), args.warmup)
+    mita.mita_device_status(ws)
+    slots = w.m + w.s * w.k
+    flops = w.BH * w.N * (2.0 * 2 * slots * w.d + 2.0 * 3 * slots * w.d) + w.BH * 8.0 * 2 * w.m * w.N * w.d
+    sm_mhz = 2070.0
+    peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+    print(json.dumps({"workload": "longctx_n32k B1 H2 (backward)", "ms": ms, "unit": "ms per backward",
+                      "flops": flops, "achieved_tflops": flops / (ms * 1e-3) / 1e12, "bound": "alu",
+                      "peak_tflops": peak, "frac": flops / (ms * 1e-3) / 1e12 / peak,
+                      "peak_source": "152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz"}), flush=True)
 
 
 def e2e_run(mita, p, Qn, Kn, Vn, w, dev, steps, dist, world):

@@ -5,6 +5,7 @@ kernels of ``libmita.so``; PyTorch supplies device memory and the stream. The
 entry points carry the names of the C ABI in ``include/mita.h``:
 ``mita_workspace_size``, ``mita_landmarks``, ``mita_select``,
 ``mita_forward``, ``mita_host_buffer_size``, ``mita_forward_host``,
+``mita_forward_static``, ``mita_backward_workspace_size``, ``mita_backward``,
 ``mita_device_status``, ``mita_uses_tensor_cores``.
 
 The library must be built first (``python -c "import __graft_entry__ as g;
@@ -87,6 +88,10 @@ def lib():
         L.mita_last_error.argtypes = []
         L.mita_last_error.restype = ctypes.c_char_p
         L.mita_uses_tensor_cores.argtypes = [P]
+        L.mita_backward_workspace_size.argtypes = [P]
+        L.mita_backward_workspace_size.restype = sz
+        L.mita_backward.argtypes = [P, vp, vp, vp, vp, ip, ip, vp, vp, vp, vp, sz, vp]
+        L.mita_backward.restype = ctypes.c_int
         L.mita_forward_static.argtypes = [P, vp, vp, vp, vp, ip, vp]
         L.mita_forward_static.restype = ctypes.c_int
         L.mita_launch_count.argtypes = []
@@ -188,6 +193,32 @@ def mita_forward_host(p: Params, Q, K, V, O, dev, stream=None):
     buffer of mita_host_buffer_size(p) bytes."""
     _check(lib().mita_forward_host(ctypes.byref(p.c()), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dev), dev.numel(),
                                    _stream(stream)))
+
+
+def mita_backward_workspace_size(p: Params) -> int:
+    return int(lib().mita_backward_workspace_size(ctypes.byref(p.c())))
+
+
+def mita_backward(p: Params, Q, K, V, dO, idx, route, dQ, dK, dV, ws, stream=None):
+    _check(lib().mita_backward(ctypes.byref(p.c()), _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(idx), _ptr(route),
+                               _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def backward(Q, K, V, dO, idx, route, m, k, s, scale=0.0, flags=0, ws=None):
+    """Gradients (dQ, dK, dV) of sum(O * dO) for the forward pass with expert
+    sets idx [B, H, m, k] and routes route [B, H, N, s] (torch CUDA tensors);
+    the sets and routes are held fixed."""
+    import torch
+    p = params_for(Q, m, k, s, None, None, scale, flags)
+    if ws is None:
+        n = mita_backward_workspace_size(p)
+        if n == 0:
+            raise MitaError(2, lib().mita_last_error().decode() or "unsupported parameters")
+        ws = torch.empty(n, dtype=torch.uint8, device=Q.device)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    mita_backward(p, Q, K, V, dO, idx, route, dQ, dK, dV, ws)
+    mita_device_status(ws)
+    return dQ, dK, dV
 
 
 def mita_device_status(ws, stream=None):

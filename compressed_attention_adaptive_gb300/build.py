@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmita.so")
-SOURCES = ["api.cu", "simt.cu", "select.cu", "tc.cu", "static_ws.cu"]
+SOURCES = ["api.cu", "simt.cu", "select.cu", "tc.cu", "static_ws.cu", "backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC,-O2",
          "-I" + os.path.join(ROOT, "include")]

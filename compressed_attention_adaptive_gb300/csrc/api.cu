@@ -254,6 +254,40 @@ mita_status forward_on_workspace(const mita_params* p, const void* Q, const void
     return run(p, Q, K, V, O, nullptr, nullptr, nullptr, nullptr, ws, ws_bytes, stream, 2);
 }
 
+// ---------------------------------------------------------------- backward
+
+static mita_status resolve_bwd(const mita_params* p, Dims* D) {
+    mita_status st = resolve(p, D);
+    if (st) return st;
+    if (D->causal) return fail(MITA_ERR_UNSUPPORTED, "the backward pass has no causal variant");
+    if (D->gh != 1) return fail(MITA_ERR_UNSUPPORTED, "the backward pass supports 1-D pooling only");
+    if (bwd_query_smem(*D) > 200 * 1024) return fail(MITA_ERR_UNSUPPORTED, "m + s*k too large for the backward pass");
+    return MITA_OK;
+}
+
+// Carving of the backward workspace (status word first, like the forward's).
+static BwdWork carve_bwd(const Dims& D, void* ws, size_t* bytes, int** status) {
+    Carver c(ws);
+    BwdWork w{};
+    const size_t BH = D.BH, N = D.N, d = D.d, m = D.m;
+    *status = c.take<int>(64);
+    w.Qt = c.take<float>(BH * m * d);
+    w.Vt = c.take<float>(BH * m * d);
+    w.stats = c.take<float2>(BH * m);
+    w.S = c.take<float>(BH * m * N);
+    w.dA = c.take<float>(BH * m * N);
+    w.Psh = c.take<float>(BH * N * m);
+    w.dZsh = c.take<float>(BH * N * m);
+    w.dQt = c.take<float>(BH * m * d);
+    w.dVt = c.take<float>(BH * m * d);
+    w.delta = c.take<float>(BH * m);
+    w.dQacc = c.take<float>(BH * N * d);
+    w.dKacc = c.take<float>(BH * N * d);
+    w.dVacc = c.take<float>(BH * N * d);
+    *bytes = align_up(c.off, 1024);
+    return w;
+}
+
 }  // namespace mita
 
 using namespace mita;
@@ -455,6 +489,40 @@ int mita_profile_end(char* names, size_t names_bytes, double* ms, int max_phases
         names[c] = 0;
     }
     return n;
+}
+
+size_t mita_backward_workspace_size(const mita_params* p) {
+    Dims D;
+    if (resolve_bwd(p, &D)) return 0;
+    size_t bytes;
+    int* st;
+    carve_bwd(D, nullptr, &bytes, &st);
+    return bytes;
+}
+
+mita_status mita_backward(const mita_params* p, const void* Q, const void* K, const void* V, const void* dO,
+                          const int32_t* idx, const int32_t* route, void* dQ, void* dK, void* dV, void* ws,
+                          size_t ws_bytes, void* stream) {
+    g_last_error.clear();
+    Dims D;
+    mita_status st = resolve_bwd(p, &D);
+    if (st) return st;
+    const void* ptrs[] = {Q, K, V, dO, idx, route, dQ, dK, dV};
+    for (const void* x : ptrs)
+        if (!x || ((uintptr_t)x & 15))
+            return fail(MITA_ERR_INVALID_ARG, "tensors must be 16-byte aligned device pointers");
+    size_t need;
+    int* status;
+    carve_bwd(D, nullptr, &need, &status);
+    if (!ws) return fail(MITA_ERR_WORKSPACE, "workspace is NULL");
+    if ((uintptr_t)ws % 256) return fail(MITA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (ws_bytes < need) return fail(MITA_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+    const BwdWork w = carve_bwd(D, ws, &need, &status);
+    cudaStream_t s = (cudaStream_t)stream;
+    MITA_CUDA(cudaMemsetAsync(status, 0, sizeof(int), s), "clear the device status word");
+    MITA_CUDA(launch_backward(D, w, Q, K, V, dO, idx, route, dQ, dK, dV, status, s), "backward pass");
+    prof_mark(s, "");
+    return MITA_OK;
 }
 
 int mita_uses_tensor_cores(const mita_params* p) {

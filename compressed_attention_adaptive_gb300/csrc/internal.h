@@ -95,3 +95,21 @@ cudaError_t launch_forward_tc(const Dims& D, const TcPlan& P, const TcWork& W, c
                               cudaStream_t st);
 
 }  // namespace mita
+
+namespace mita {
+
+// backward.cu: workspace of the backward pass (fp32 throughout).
+struct BwdWork {
+    float *Qt, *Vt;             // [BH][m][d] landmarks and shared expert again
+    float2* stats;              // [BH][m] row max of scale * s and 1 / row sum of the shared expert
+    float *S, *dA;              // [BH][m][N] raw landmark scores (then A) and dA (then dS)
+    float *Psh, *dZsh;          // [BH][N][m] the shared slots' P and dZ per query
+    float *dQt, *dVt, *delta;   // [BH][m][d], [BH][m][d], [BH][m]
+    float *dQacc, *dKacc, *dVacc;  // [BH][N][d] fp32 accumulators
+};
+size_t bwd_query_smem(const Dims& D);
+cudaError_t launch_backward(const Dims& D, const BwdWork& W, const void* Q, const void* K, const void* V,
+                            const void* dO, const int32_t* I, const int32_t* E, void* dQ, void* dK, void* dV,
+                            int* status, cudaStream_t st);
+
+}  // namespace mita

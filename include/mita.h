@@ -158,6 +158,31 @@ const char* mita_status_string(mita_status s);
 /* Detail of the last error returned on the calling thread ("" if none). */
 const char* mita_last_error(void);
 
+/* ---- backward pass ---------------------------------------------------------
+ * The summaries describe the forward pass and report training speed, but print
+ * no backward pass; this one is the chain rule through the forward's steps with
+ * the expert sets and routes held fixed (a top-k choice is piecewise constant
+ * and has no gradient): through each query's softmax over its shared and
+ * routed slots, through the shared expert Vt = softmax(scale Qt K^T) V, and
+ * through the pooling of the landmarks. Runs on CUDA cores in fp32 (the inputs
+ * widened from `dtype`). Non-causal, 1-D pooling only (other settings return
+ * MITA_ERR_UNSUPPORTED).
+ *
+ * Bytes of device workspace mita_backward() needs for `p`; 0 if `p` is invalid
+ * or unsupported there. */
+size_t mita_backward_workspace_size(const mita_params* p);
+
+/* Gradients of sum(O * dO) with respect to Q, K, V. Q, K, V, dO and the
+ * outputs dQ, dK, dV: device [B, H, N, d] in `dtype`; idx [B, H, m, k] and
+ * route [B, H, N, s]: the expert sets and routes of the forward pass whose
+ * gradient is wanted (mita_forward's idx_out / route_out, or mita_select's).
+ * Every output row is written. Asynchronous on `stream`; argument errors are
+ * returned before anything is enqueued; an index out of range in idx or route
+ * is recorded in the workspace's status word (mita_device_status on `ws`). */
+mita_status mita_backward(const mita_params* p, const void* Q, const void* K, const void* V, const void* dO,
+                          const int32_t* idx, const int32_t* route, void* dQ, void* dK, void* dV, void* ws,
+                          size_t ws_bytes, void* stream);
+
 /* 1 if `p` runs on the tcgen05 tensor-core path, 0 if on CUDA cores, -1 if invalid. */
 int mita_uses_tensor_cores(const mita_params* p);
 

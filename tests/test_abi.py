@@ -82,3 +82,12 @@ def test_causal_flag_validation(lib):
     assert mita.mita_workspace_size(_p(flags=C, k=512)) == 0                              # unsupported on tcgen05
     assert mita.mita_workspace_size(_p(flags=C | mita.FLAG_SIMT, k=512)) > 0               # CUDA cores run it
     assert mita.mita_workspace_size(_p(flags=C, dtype=mita.F32, k=512)) > 0
+
+
+def test_backward_workspace_and_validation(lib):
+    assert mita.mita_backward_workspace_size(_p()) > 0
+    assert mita.mita_backward_workspace_size(_p(flags=mita.FLAG_CAUSAL)) == 0                     # no causal backward
+    assert mita.mita_backward_workspace_size(_p(grid_h=32, grid_w=32, lm_h=4, lm_w=4)) == 0       # 1-D pooling only
+    p = _p()
+    rc = lib.mita_backward(ctypes.byref(p.c()), *([None] * 9), None, 0, None)
+    assert rc == 1 and b"aligned" in lib.mita_last_error()
