@@ -564,8 +564,10 @@ def backward_arm(args):
     p = mita.params_for(Q, w.m, w.k, w.s)
     ws = torch.empty(mita.mita_backward_workspace_size(p), dtype=torch.uint8, device=dev)
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
-    ms = _time_cuda(lambda: mita.mita_backward(p, Q, K, V, dO, idx, route, dQ, dK, dV, ws),
-                    max(3, min(args.steps, 10)), args.warmup)
+    steps = max(3, min(args.steps, 10))
+    mita.mita_profile_begin(16 * (steps + args.warmup) + 16)
+    ms = _time_cuda(lambda: mita.mita_backward(p, Q, K, V, dO, idx, route, dQ, dK, dV, ws), steps, args.warmup)
+    phases = {k_: v_ / (steps + args.warmup) for k_, v_ in mita.mita_profile_end().items()}
     mita.mita_device_status(ws)
     slots = w.m + w.s * w.k
     flops = w.BH * w.N * (2.0 * 2 * slots * w.d + 2.0 * 3 * slots * w.d) + w.BH * 8.0 * 2 * w.m * w.N * w.d
@@ -574,7 +576,8 @@ def backward_arm(args):
     print(json.dumps({"workload": "longctx_n32k B1 H2 (backward)", "ms": ms, "unit": "ms per backward",
                       "flops": flops, "achieved_tflops": flops / (ms * 1e-3) / 1e12, "bound": "alu",
                       "peak_tflops": peak, "frac": flops / (ms * 1e-3) / 1e12 / peak,
-                      "peak_source": "152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz"}), flush=True)
+                      "peak_source": "152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",
+                      "phases_ms": phases}), flush=True)
 
 
 def e2e_run(mita, p, Qn, Kn, Vn, w, dev, steps, dist, world):

@@ -262,6 +262,7 @@ static mita_status resolve_bwd(const mita_params* p, Dims* D) {
     if (D->causal) return fail(MITA_ERR_UNSUPPORTED, "the backward pass has no causal variant");
     if (D->gh != 1) return fail(MITA_ERR_UNSUPPORTED, "the backward pass supports 1-D pooling only");
     if (bwd_query_smem(*D) > 200 * 1024) return fail(MITA_ERR_UNSUPPORTED, "m + s*k too large for the backward pass");
+    if (D->d != 64 && D->d != 128) return fail(MITA_ERR_UNSUPPORTED, "the backward pass supports d = 64 or 128");
     return MITA_OK;
 }
 
@@ -284,6 +285,12 @@ static BwdWork carve_bwd(const Dims& D, void* ws, size_t* bytes, int** status) {
     w.dQacc = c.take<float>(BH * N * d);
     w.dKacc = c.take<float>(BH * N * d);
     w.dVacc = c.take<float>(BH * N * d);
+    w.Pr = c.take<float>(BH * N * D.s * (size_t)D.k);
+    w.dZr = c.take<float>(BH * N * D.s * (size_t)D.k);
+    w.counts = c.take<int>(BH * m);
+    w.cursors = c.take<int>(BH * m);
+    w.offs = c.take<int>(BH * (m + 1));
+    w.rows = c.take<int>(BH * N * D.s);
     *bytes = align_up(c.off, 1024);
     return w;
 }

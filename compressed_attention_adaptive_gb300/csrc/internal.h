@@ -33,6 +33,8 @@ cudaError_t launch_select_simt(const Dims& D, const void* Q, const void* K, cons
                                int32_t* I, int32_t* E, cudaStream_t st);
 cudaError_t launch_shared_simt(const Dims& D, const void* V, const float* S, float2* stats, float* Vt,
                                cudaStream_t st);
+// per landmark row of raw scores S: (max of scale * s, 1 / sum exp(scale * s - max))
+cudaError_t launch_row_stats(const Dims& D, const float* S, float2* stats, cudaStream_t st);
 size_t out_simt_smem(const Dims& D);
 cudaError_t launch_out_simt(const Dims& D, const void* Q, const void* K, const void* V, const float* Qt,
                             const float* Vt, const int32_t* I, const int32_t* E, void* O, int* status,
@@ -106,6 +108,9 @@ struct BwdWork {
     float *Psh, *dZsh;          // [BH][N][m] the shared slots' P and dZ per query
     float *dQt, *dVt, *delta;   // [BH][m][d], [BH][m][d], [BH][m]
     float *dQacc, *dKacc, *dVacc;  // [BH][N][d] fp32 accumulators
+    float *Pr, *dZr;            // [BH][N][s][k] the routed slots' P and dZ per query
+    int *counts, *cursors;      // [BH][m] bucket sizes and scatter cursors
+    int *offs, *rows;           // [BH][m + 1] bucket offsets, [BH][N * s] pairs in bucket order
 };
 size_t bwd_query_smem(const Dims& D);
 cudaError_t launch_backward(const Dims& D, const BwdWork& W, const void* Q, const void* K, const void* V,

@@ -390,6 +390,12 @@ static cudaError_t shared_simt_t(const Dims& D, const void* V, const float* S, f
     return cudaGetLastError();
 }
 
+cudaError_t launch_row_stats(const Dims& D, const float* S, float2* stats, cudaStream_t st) {
+    k_row_softmax_stats<<<D.BH * D.m, 256, 0, st>>>(S, D.N, D.m, D.causal ? 1 : 0, D.scale, stats);
+    count_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_shared_simt(const Dims& D, const void* V, const float* S, float2* stats, float* Vt,
                                cudaStream_t st) {
     return D.dtype == 0 ? shared_simt_t<float>(D, V, S, stats, Vt, st)
