@@ -596,18 +596,25 @@ def e2e_run(mita, p, Qn, Kn, Vn, w, dev, steps, dist, world):
     hO, _ = pinned_host(nbytes, torch)
     buf = torch.empty(mita.mita_host_buffer_size(p), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    for _ in range(3):
+    for _ in range(5):
         mita.mita_forward_host(p, hb[0], hb[1], hb[2], hO, buf)
     torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-    ev[0].record(stream)
-    for i in range(steps):
-        mita.mita_forward_host(p, hb[0], hb[1], hb[2], hO, buf)
-        ev[i + 1].record(stream)
-    torch.cuda.synchronize(dev)
-    per = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+    import gc
+    gc.collect()
+    gc.disable()  # no collector pause between the enqueues of the timed steps
+    try:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record(stream)
+        for i in range(steps):
+            mita.mita_forward_host(p, hb[0], hb[1], hb[2], hO, buf)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+    finally:
+        gc.enable()
+    seq = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    per = sorted(seq)
     ms = job_max(dist, ev[0].elapsed_time(ev[steps]) / steps)
     # raw copy rates of the same pinned buffers (the floor of the end-to-end step)
     c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
@@ -623,6 +630,7 @@ def e2e_run(mita, p, Qn, Kn, Vn, w, dev, steps, dist, world):
     return {"value": world * w.BH * w.N / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": 3 * nbytes,
             "d2h_bytes_per_step": nbytes, "ms_per_step": ms, "steps": steps,
             "ms_median": per[len(per) // 2], "ms_min": per[0], "ms_max": per[-1],
+            "slowest_step": int(max(range(steps), key=lambda i: seq[i])),
             "host_buffers": how, "copy_only_h2d_gbs": h2d_gbs, "copy_only_d2h_gbs": d2h_gbs}
 
 
