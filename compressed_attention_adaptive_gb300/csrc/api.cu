@@ -160,20 +160,20 @@ static Work carve(const Dims& D, void* ws, size_t* bytes) {
         t.cand = c.take<int2>(BH * P.m_pad * (size_t)P.splits * (size_t)P.cand_cap);
         t.ccount = c.take<int>(BH * P.m_pad * (size_t)P.splits * 2);
         t.counts = c.take<int>(BH * D.m * 2);
-        t.tile_ctr = c.take<int>(2);
+        t.tile_ctr = c.take<int>(3);
         t.zero_begin = t.counts;
-        t.zero_bytes = t.counts ? (size_t)((char*)(t.tile_ctr + 2) - (char*)t.counts) : 0;
+        t.zero_bytes = t.counts ? (size_t)((char*)(t.tile_ctr + 3) - (char*)t.counts) : 0;
         t.cursors = c.take<int>(BH * D.m * 2);
         t.toff = c.take<int>(BH * D.m);
         t.tiles = c.take<int4>((size_t)P.max_tiles);
         t.xtl = c.take<int2>(BH * D.m);
         t.perm = c.take<int32_t>(BH * D.N * D.s);
-        t.part = c.take<__nv_bfloat16>(BH * D.N * D.s * D.d);
-        t.lse = c.take<float>(BH * D.N * D.s);
+        t.part = c.take<__nv_bfloat16>(BH * D.N * D.s * P.nsub * D.d);
+        t.lse = c.take<float>(BH * D.N * D.s * P.nsub);
         t.cnt = c.take<int>(BH * D.N);
-        if (P.resident) {
-            t.sh_part = c.take<__nv_bfloat16>(BH * D.N * D.d);
-            t.sh_lse = c.take<float>(BH * D.N);
+        if (P.nsh) {
+            t.sh_part = c.take<__nv_bfloat16>(BH * D.N * P.nsh * D.d);
+            t.sh_lse = c.take<float>(BH * D.N * P.nsh);
         }
     }
     *bytes = align_up(c.off, 1024);

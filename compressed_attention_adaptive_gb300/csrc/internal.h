@@ -62,7 +62,11 @@ struct TcPlan {
     int R;                 // top-k sample stride (every R-th key)
     int n_samp;            // sampled keys per row (>= k)
     long long cand_cap;    // candidate records per (row, split)
-    bool resident;         // expert keys resident in shared memory, shared slots in the routing pass
+    bool resident;         // the causal variant's tensor-core path: m <= 128, k <= 256, shared slots on
+    bool route_shared;     // the routing pass also computes the shared slots (m <= 128, shared slots on)
+    int ksub, nsub;        // keys per sub-expert (<= 256) and sub-experts per expert
+    int ksub_sh, nsub_sh;  // the same for the shared slots when they run as their own pass (m > 128)
+    int nsh;               // shared-slot partials per query (0 with the shared slots off)
 };
 
 // Workspace buffers of the tensor-core path.
@@ -75,7 +79,7 @@ struct TcWork {
     int2* cand;                      // [BH][m_pad][splits][2][cand_cap / 2] (score, key) records
     int* ccount;                     // [BH][m_pad][splits][2]
     int* counts;                     // [BH][m][2]
-    int* tile_ctr;                   // [2]: tiles written, experts claimed by the expert attention
+    int* tile_ctr;                   // [3]: tiles written, expert and shared-pass claims of the expert attention
     void* zero_begin;                // counts .. tile_ctr, cleared each call
     size_t zero_bytes;
     int* cursors;                    // [BH][m][2]
@@ -83,11 +87,11 @@ struct TcWork {
     int4* tiles;                     // [max_tiles]
     int2* xtl;                       // [BH][m] (first tile, tile count) of each expert
     int32_t* perm;                   // [BH][N*s]
-    __nv_bfloat16* part;             // [BH][N][s][d]
-    float* lse;                      // [BH][N][s]
+    __nv_bfloat16* part;             // [BH][N][s][nsub][d]
+    float* lse;                      // [BH][N][s][nsub]
     int* cnt;                        // [BH][N]
-    __nv_bfloat16* sh_part;          // [BH][N][d] shared-slot partial (resident-key path)
-    float* sh_lse;                   // [BH][N]
+    __nv_bfloat16* sh_part;          // [BH][N][nsh][d] shared-slot partials
+    float* sh_lse;                   // [BH][N][nsh]
 };
 
 bool tc_supported(const Dims& D);

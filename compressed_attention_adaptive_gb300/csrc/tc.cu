@@ -27,9 +27,6 @@ using namespace tc;
 namespace {
 
 constexpr int kT = 128;                     // rows per tile = keys per chunk
-constexpr int kPTile = kT * kT * 2;         // P tile bytes (128 x 128 bf16)
-// K buffer that the P tile reuses: large enough for either.
-template <int D> constexpr int kp_bytes() { return kT * D * 2 > kPTile ? kT * D * 2 : kPTile; }
 constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);  // S[128 x 128] = A[128 x d] B[128 x d]^T
 
 __device__ __forceinline__ uint32_t lane_base(uint32_t tmem) { return tmem + ((threadIdx.x & 96u) << 16); }
@@ -101,19 +98,6 @@ __device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t sA, uint32_t sB, 
         const uint32_t off = (kk >> 2) * kT * 128 + (kk & 3) * 32;
         mma_bf16(tS, sdesc(sA + off, 16, 1024), sdesc(sB + off, 16, 1024), kIdS,
                  (kk > 0 || accumulate_first) ? 1u : 0u);
-    }
-}
-
-// Issues O (+)= P * V: P is a K-major 128 x 128 tile, V an MN-major
-// 128 keys x D tile (D contiguous).
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t sP, uint32_t sV, bool accumulate) {
-    constexpr uint32_t id = idesc_bf16(128, D, 0, 1);
-#pragma unroll
-    for (int kk = 0; kk < kT / 16; ++kk) {
-        const uint32_t offp = (kk >> 2) * kT * 128 + (kk & 3) * 32;
-        mma_bf16(tO, sdesc(sP + offp, 16, 1024), sdesc(sV + kk * 2048, kT * 128, 1024), id,
-                 (kk > 0 || accumulate) ? 1u : 0u);
     }
 }
 
@@ -1204,11 +1188,73 @@ __global__ void k_bucket_scatter(const int32_t* __restrict__ E, int N, int m, in
         if (bin[t] >= 0) perm[(size_t)bh * N * s + bins[bin[t]] + rank[t]] = (q << 3) | t;
 }
 
-// Output rows from the partials: each query's s expert partials (normalized
-// bf16 rows with log2-sum-exp) and, when given, its shared-slot partial,
-// weighted by 2^(lse - max). One thread per 8 columns of a query.
+// Output rows from the partials: each query's ne expert partials (normalized
+// bf16 rows with their log2-sum-exp; the s routed slots times their
+// sub-experts) and its ns shared-slot partials, weighted by 2^(lse - max): the
+// softmax over the union of the partials' keys. One thread per 8 columns of a
+// query; the partials come in groups of four, all loads of a group in flight
+// at once, with an online rescale when a later group raises the maximum.
 template <int D>
 __global__ void __launch_bounds__(256) k_merge(const __nv_bfloat16* __restrict__ part, const float* __restrict__ lse,
+                                               int ne, const __nv_bfloat16* __restrict__ sh_part,
+                                               const float* __restrict__ sh_lse, int ns, __nv_bfloat16* __restrict__ O,
+                                               long long nq) {
+    constexpr int G = D / 8;   // threads per query
+    constexpr int kGrp = 4;    // partials per group
+    const long long qi = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / G;
+    const int gcol = (threadIdx.x % G) * 8;
+    if (qi >= nq) return;
+    float L = -INFINITY, wsum = 0.0f;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int j0 = 0; j0 < ne + ns; j0 += kGrp) {
+        uint4 raw[kGrp];
+        float lj[kGrp];
+#pragma unroll
+        for (int j = 0; j < kGrp; ++j) {
+            const int t = j0 + j;
+            lj[j] = -INFINITY;
+            if (t < ne) {
+                lj[j] = lse[qi * ne + t];
+                raw[j] = *reinterpret_cast<const uint4*>(part + (qi * ne + t) * D + gcol);
+            } else if (t < ne + ns) {
+                lj[j] = sh_lse[qi * ns + (t - ne)];
+                raw[j] = *reinterpret_cast<const uint4*>(sh_part + (qi * ns + (t - ne)) * D + gcol);
+            }
+        }
+        float gm = lj[0];
+#pragma unroll
+        for (int j = 1; j < kGrp; ++j) gm = fmaxf(gm, lj[j]);
+        if (gm > L) {  // rescale what earlier groups added (nothing before the first real partial)
+            const float a = L > -INFINITY ? exp2f(L - gm) : 0.0f;
+            wsum *= a;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] *= a;
+            L = gm;
+        }
+#pragma unroll
+        for (int j = 0; j < kGrp; ++j) {
+            if (!(lj[j] > -INFINITY)) continue;  // absent, or empty (causal only): weighs 0
+            const float w = exp2f(lj[j] - L);
+            wsum += w;
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const float2 f = __bfloat1622float2(h[v]);
+                acc[2 * v] = fmaf(w, f.x, acc[2 * v]);
+                acc[2 * v + 1] = fmaf(w, f.y, acc[2 * v + 1]);
+            }
+        }
+    }
+    const float winv = wsum > 0.0f ? 1.0f / wsum : 0.0f;  // no slot at all (causal only): a zero row
+    *reinterpret_cast<uint4*>(O + qi * D + gcol) =
+        make_uint4(pack_bf16(acc[0] * winv, acc[1] * winv), pack_bf16(acc[2] * winv, acc[3] * winv),
+                   pack_bf16(acc[4] * winv, acc[5] * winv), pack_bf16(acc[6] * winv, acc[7] * winv));
+}
+
+// The common case of the merge below (at most kMaxS expert partials and at
+// most one shared partial): every load of a query in flight at once.
+template <int D>
+__global__ void __launch_bounds__(256) k_merge_few(const __nv_bfloat16* __restrict__ part, const float* __restrict__ lse,
                                                const __nv_bfloat16* __restrict__ sh_part,
                                                const float* __restrict__ sh_lse, __nv_bfloat16* __restrict__ O,
                                                long long nq, int s) {
@@ -1250,419 +1296,25 @@ __global__ void __launch_bounds__(256) k_merge(const __nv_bfloat16* __restrict__
                    pack_bf16(acc[4] * winv, acc[5] * winv), pack_bf16(acc[6] * winv, acc[7] * winv));
 }
 
-// The last-finisher merge of a query's s partial outputs: publish this
-// partial's log2-sum-exp, count it, and if it is the query's last, combine
-// all s normalized partials (read back from L2) into the output row.
-template <int D>
-__device__ __forceinline__ void merge_partials(__nv_bfloat16* __restrict__ O, __nv_bfloat16* __restrict__ part,
-                                               float* __restrict__ lse, int* __restrict__ cnt, int bh, int N, int q,
-                                               int s, size_t pr, float my_lse) {
-    lse[pr] = my_lse;
-    // release this partial (row and lse) and, if last, acquire the others
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(cnt + (size_t)bh * N + q) : "memory");
-    if (old != s - 1) return;
-    const size_t p0 = ((size_t)bh * N + q) * s;
-    float lj[kMaxS];
-    float L = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kMaxS; ++j) {
-        lj[j] = j < s ? __ldcg(lse + p0 + j) : -INFINITY;
-        L = fmaxf(L, lj[j]);
-    }
-    float acc[D];
-#pragma unroll
-    for (int c = 0; c < D; ++c) acc[c] = 0.0f;
-    float wsum = 0.0f;
-    for (int j = 0; j < s; ++j) {
-        const float w = exp2f(lj[j] - L);
-        wsum += w;
-        // the whole partial row in flight at once
-        const uint4* src = reinterpret_cast<const uint4*>(part + (p0 + j) * D);
-        uint4 raw[D / 8];
-#pragma unroll
-        for (int u = 0; u < D / 8; ++u) raw[u] = __ldcg(src + u);
-#pragma unroll
-        for (int u = 0; u < D / 8; ++u) {
-            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const float2 f = __bfloat1622float2(h[v]);
-                acc[8 * u + 2 * v] = fmaf(w, f.x, acc[8 * u + 2 * v]);
-                acc[8 * u + 2 * v + 1] = fmaf(w, f.y, acc[8 * u + 2 * v + 1]);
-            }
-        }
-    }
-    const float winv = 1.0f / wsum;
-    uint4* od = reinterpret_cast<uint4*>(O + ((size_t)bh * N + q) * D);
-#pragma unroll
-    for (int u = 0; u < D / 8; ++u)
-        od[u] = make_uint4(pack_bf16(acc[8 * u] * winv, acc[8 * u + 1] * winv),
-                           pack_bf16(acc[8 * u + 2] * winv, acc[8 * u + 3] * winv),
-                           pack_bf16(acc[8 * u + 4] * winv, acc[8 * u + 5] * winv),
-                           pack_bf16(acc[8 * u + 6] * winv, acc[8 * u + 7] * winv));
-}
-
-// ------------------------------------------------------------------------
-// Expert attention, warp-specialized and persistent (one CTA per SM).
-//   warps 0-3  softmax + epilogue, thread r <-> TMEM lane r (row r of a tile)
-//   warp 4     producer: claims work tiles, gathers the tile's queries and each
-//              chunk's keys / values (rows picked by index) with cp.async,
-//              completion counted on mbarriers
-//   warp 5     MMA issuer: S = Q K^T into one of two TMEM score buffers, and
-//              O += P V into one of two TMEM output buffers (one per tile in
-//              flight); S of chunk g+1 runs while the softmax works on chunk g
-// Shared memory: 2 query tiles and a 2-stage ring of (K, V) chunks; once S of
-// a chunk is in TMEM its K slot holds the chunk's probabilities P (bf16).
-// Every wait is bounded; a timeout sets the device status and an abort flag
-// that makes every role leave its loop.
-
-struct WsTile {
-    int bh, e, rows, shrows, nsh, nch;
-};
-
-struct WsMeta {  // what the deferred O += P V of a chunk needs
-    int st, ob, tseq;
-    bool first, last;
-};
-
-// producer warps of the expert-attention kernels (they share the gathers of
-// query rows and keys / values); streaming kernel: warps 0-3 softmax +
-// epilogue, 4 .. 4 + kNPW - 1 producers, then the MMA warp
-constexpr int kNPW = 3, kWsThreads = 32 * (4 + kNPW + 1);
-
-template <int D>
-__global__ void __launch_bounds__(kWsThreads, 1)
-    k_expert_ws(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
-                const __nv_bfloat16* __restrict__ V, const __nv_bfloat16* __restrict__ Qhi,
-                const __nv_bfloat16* __restrict__ Vtb, const int32_t* __restrict__ I,
-                const int32_t* __restrict__ perm, const int4* __restrict__ tiles, const int* __restrict__ tile_ctr,
-                __nv_bfloat16* __restrict__ O, __nv_bfloat16* __restrict__ part,
-                float* __restrict__ lse, int* __restrict__ cnt, int N, int m, int m_pad, int k, int s, int shared_on,
-                float sl, int* __restrict__ status) {
-    constexpr int TILE = kT * D * 2;
-    constexpr uint32_t kS0 = 0, kO0 = 256;  // TMEM columns: S buffers 0 / 128, O buffers 256 / 384
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    constexpr int KP = kp_bytes<D>();  // K stage, later the P tile
-    uint8_t* sQ = sm;                  // 2 tiles
-    uint8_t* sK = sm + 2 * TILE;       // 2 stages of KP bytes
-    uint8_t* sV = sK + 2 * KP;         // 2 stages
-
-    __shared__ uint64_t q_full[2], q_empty[2], kv_full[2], kv_empty[2], s_full[2], s_free[2], o_full[2], o_free[2];
-    __shared__ uint64_t p_full[2], pv_done;  // p_full[g & 1]: the softmax may run two chunks ahead of O += P V
-    __shared__ WsTile tinfo[2];
-    __shared__ int rowq[2][kT];  // q << 3 | slot, or -1
-    __shared__ int keyrow[2][kT];  // producer: key rows of the chunk being loaded / the next one
-    __shared__ uint32_t tmem_slot;
-    __shared__ int abort_flag;
-    volatile int* abort_v = &abort_flag;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ntiles = *(volatile const int*)tile_ctr;
-    const int per = (ntiles + gridDim.x - 1) / gridDim.x;
-    const int t_begin = blockIdx.x * per, nloc = max(0, min(ntiles, t_begin + per) - t_begin);
-    if (nloc == 0) return;
-    if (warp == 4 + kNPW) tmem_alloc(&tmem_slot, 512);
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&q_full[i], 33 * kNPW);  // per producer warp: 32 copy completions + the row publish
-            mbar_init(&q_empty[i], 1 + 4);
-            mbar_init(&kv_full[i], 32 * kNPW);
-            mbar_init(&kv_empty[i], 1);
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 4);
-            mbar_init(&o_full[i], 1);
-            mbar_init(&o_free[i], 4);
-        }
-        mbar_init(&p_full[0], 4);
-        mbar_init(&p_full[1], 4);
-        mbar_init(&pv_done, 1);
-        abort_flag = 0;
-        fence_mbar_init();
-    }
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    const uint32_t tmem = tmem_slot;
-    const int nex = (k + kT - 1) / kT;
-    const int nsh_full = shared_on ? (m + kT - 1) / kT : 0;
-
-    if (warp >= 4 && warp < 4 + kNPW) {
-        // ------------------------------------------------------- producers
-        // all kNPW warps gather (row pairs dealt round-robin); the first also
-        // writes the tile info
-        const int pw = warp - 4;
-        int g = 0;
-        for (int tseq = 0; tseq < nloc; ++tseq) {
-            const int qs = tseq & 1;
-            int ok = 1;
-            if (lane == 0) ok = ws_wait(&q_empty[qs], ((tseq >> 1) & 1) ^ 1, status, abort_v);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            const int4 td = tiles[t_begin + tseq];
-            const int bh = td.x, e = td.y, start = td.z, rows = td.w & 255, shrows = td.w >> 8;
-            const int nsh = shrows > 0 ? nsh_full : 0;
-            const int nch = nsh + nex;
-            // row indices go to shared memory; the copies then run two rows per
-            // warp instruction (16 lanes x 16 bytes per 256-byte row for d = 128)
-            const int rbase = bh * N;
-            constexpr int CPR = D / 8;        // 16-byte chunks per row
-            constexpr int RPI = 32 / CPR;     // rows per warp instruction
-            for (int r = lane; r < kT; r += 32)
-                if ((r / RPI) % kNPW == pw) rowq[qs][r] = r < rows ? perm[(size_t)bh * N * s + start + r] : -1;
-            if (pw == 0 && lane == 0) tinfo[qs] = WsTile{bh, e, rows, shrows, nsh, nch};
-            __syncwarp();
-            {
-                const uint32_t dst = smem_u32(sQ + qs * TILE);
-                const int cc = lane % CPR;
-#pragma unroll 4
-                for (int r0 = pw * RPI; r0 < kT; r0 += kNPW * RPI) {
-                    const int r = r0 + lane / CPR;
-                    const int pk = rowq[qs][r];
-                    const __nv_bfloat16* src = Q + ((size_t)rbase + (pk >= 0 ? (pk >> 3) : 0)) * D + cc * 8;
-                    cp_async16(dst + sw_off(r, cc, kT), src, true);
-                }
-                cp_async_arrive(&q_full[qs]);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&q_full[qs]);  // publishes this warp's rowq rows (and tinfo)
-            }
-            // key rows of chunk c into keyrow[buf]: landmark rows for the shared
-            // chunks, I_e entries for the expert's chunks
-            auto load_keys = [&](int c, int buf) {
-                const bool shc = c < nsh;
-                for (int r = lane; r < kT; r += 32) {
-                    if ((r / RPI) % kNPW != pw) continue;  // this warp's rows only
-                    int row;
-                    if (shc) {
-                        row = c * kT + r;  // < m_pad since c < ceil(m / 128)
-                    } else {
-                        const int t2 = (c - nsh) * kT + r;
-                        int j = t2 < k ? I[((size_t)bh * m + e) * k + t2] : 0;
-                        if (j < 0 || j >= N) {
-                            set_status(status, kStBounds);
-                            j = 0;
-                        }
-                        row = j;
-                    }
-                    keyrow[buf][r] = row;
-                }
-            };
-            load_keys(0, g & 1);
-            bool ok2 = true;
-            for (int c = 0; c < nch; ++c, ++g) {
-                const int st = g & 1;
-                int okw = 1;
-                if (lane == 0) okw = ws_wait(&kv_empty[st], ((g >> 1) & 1) ^ 1, status, abort_v);
-                if (!__shfl_sync(0xffffffffu, okw, 0)) { ok2 = false; break; }
-                __syncwarp();
-                {
-                    const bool shc = c < nsh;
-                    const __nv_bfloat16* kb = shc ? Qhi + (size_t)bh * m_pad * D : K + (size_t)rbase * D;
-                    const __nv_bfloat16* vb = shc ? Vtb + (size_t)bh * m_pad * D : V + (size_t)rbase * D;
-                    const uint32_t dk = smem_u32(sK + st * KP), dv = smem_u32(sV + st * TILE);
-                    const int* kr = keyrow[g & 1];
-                    const int cc = lane % CPR;
-#pragma unroll 4
-                    for (int r0 = pw * RPI; r0 < kT; r0 += kNPW * RPI) {
-                        const int r = r0 + lane / CPR;
-                        const size_t off = (size_t)kr[r] * D + cc * 8;
-                        cp_async16(dk + sw_off(r, cc, kT), kb + off, true);
-                        cp_async16(dv + sw_off(r, cc, kT), vb + off, true);
-                    }
-                    cp_async_arrive(&kv_full[st]);
-                }
-                // the next chunk's key rows load while this stage fills and the next one drains
-                if (c + 1 < nch) load_keys(c + 1, (g + 1) & 1);
-                __syncwarp();
-            }
-            if (!ok2) break;
-        }
-        cp_async_wait_all();  // nothing of ours may still be in flight when the CTA exits
-    } else if (warp == 4 + kNPW) {
-        // ------------------------------------------------------ MMA issuer
-        // strict order: S(g), then the deferred O += P V of chunk g-1, so the
-        // tensor core computes S(g) while the softmax works on chunk g-1;
-        // every wait blocks in hardware (no spinning next to the softmax warps)
-        if (lane == 0) {
-            int g = 0, tseq = 0;
-            bool pending = false, ok = true;
-            WsMeta pm{};
-            int pg = 0;
-            auto flush_pv = [&]() -> bool {
-                if (!ws_wait(&p_full[pg & 1], (pg >> 1) & 1, status, abort_v)) return false;
-                if (pm.first && !ws_wait(&o_free[pm.ob], ((pm.tseq >> 1) & 1) ^ 1, status, abort_v)) return false;
-                fence_after_sync();
-                issue_pv<D>(tmem + kO0 + pm.ob * 128, smem_u32(sK + pm.st * KP), smem_u32(sV + pm.st * TILE),
-                            !pm.first);
-                mma_commit(&pv_done);
-                mma_commit(&kv_empty[pm.st]);
-                if (pm.last) mma_commit(&o_full[pm.ob]);
-                pending = false;
-                return true;
-            };
-            for (; tseq < nloc;) {
-                const int qs = tseq & 1;
-                if (!(ok = ws_wait(&q_full[qs], (tseq >> 1) & 1, status, abort_v))) break;
-                const WsTile ti = tinfo[qs];
-                if (ti.rows < 0) break;
-                for (int c = 0; c < ti.nch; ++c, ++g) {
-                    const int st = g & 1, sb = g & 1;
-                    if (!(ok = ws_wait(&kv_full[st], (g >> 1) & 1, status, abort_v))) break;
-                    if (!(ok = ws_wait(&s_free[sb], ((g >> 1) & 1) ^ 1, status, abort_v))) break;
-                    fence_proxy_async();  // copied tiles (generic proxy) -> the MMA's async-proxy reads
-                    fence_after_sync();
-                    issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sQ + qs * TILE), smem_u32(sK + st * KP), false);
-                    mma_commit(&s_full[sb]);
-                    const bool last = c == ti.nch - 1;
-                    if (last) mma_commit(&q_empty[qs]);
-                    if (pending && !(ok = flush_pv())) break;
-                    pending = true;
-                    pg = g;
-                    pm = WsMeta{st, tseq & 1, tseq, c == 0, last};
-                }
-                if (!ok) break;
-                ++tseq;
-            }
-            if (ok && pending) flush_pv();
-        }
-        __syncwarp();
-    } else {
-        // -------------------------------------------- softmax + epilogue
-        const int r = threadIdx.x;
-        int tseq = 0, g = 0;
-        for (; tseq < nloc;) {
-            const int qs = tseq & 1, ob = tseq & 1;
-            if (!__all_sync(0xffffffffu, ws_wait(&q_full[qs], (tseq >> 1) & 1, status, abort_v))) break;
-            const WsTile ti = tinfo[qs];
-            if (ti.rows < 0) break;
-            const int pk = rowq[qs][r];
-            const int q = pk >= 0 ? pk >> 3 : -1, slot = pk >= 0 ? pk & 7 : 0;
-            float mref = -INFINITY, l = 0.0f;
-            bool ok = true;
-            for (int c = 0; c < ti.nch; ++c, ++g) {
-                const int sb = g & 1;
-                if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (g >> 1) & 1, status, abort_v))) { ok = false; break; }
-                fence_after_sync();
-                const bool shc = c < ti.nsh;
-                const int nk = shc ? min(kT, m - c * kT) : min(kT, k - (c - ti.nsh) * kT);
-                const bool row_ok = q >= 0 && (!shc || r < ti.shrows);
-                const uint32_t tS = lane_base(tmem) + kS0 + sb * 128;
-                const uint32_t tO = lane_base(tmem) + kO0 + ob * 128;
-                // the whole score row in registers: four loads, one wait
-                float v[kT];
-                tmem_ld32(tS, v);
-                tmem_ld32(tS + 32, v + 32);
-                tmem_ld32(tS + 64, v + 64);
-                tmem_ld32(tS + 96, v + 96);
-                tmem_wait_ld();
-                fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_free[sb]);  // S(g) is read: its buffer may take S(g+2)
-                const int nval = row_ok ? nk : 0;  // columns of this row that hold a valid key
-                float mx = -INFINITY;
-#pragma unroll
-                for (int j = 0; j < kT; ++j) mx = fmaxf(mx, j < nval ? v[j] * sl : -INFINITY);
-                float mnew = mref, alpha = 1.0f;
-                if (mx > mref + 8.0f) {
-                    mnew = mx;
-                    alpha = ex2(mref - mnew);
-                }
-                uint8_t* sPg = sK + (g & 1) * KP;  // K of this chunk is consumed: P goes there
-                float sum = 0.0f;
-#pragma unroll
-                for (int c0 = 0; c0 < kT; c0 += 32) {
-                    uint32_t pkd[16];
-#pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        // exponentiate every column, keep the valid ones (no branches)
-                        const float e0 = ex2(fmaf(v[c0 + j], sl, -mnew));
-                        const float e1 = ex2(fmaf(v[c0 + j + 1], sl, -mnew));
-                        const float p0 = c0 + j < nval ? e0 : 0.0f;
-                        const float p1 = c0 + j + 1 < nval ? e1 : 0.0f;
-                        sum += p0 + p1;
-                        pkd[j >> 1] = pack_bf16(p0, p1);
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        *reinterpret_cast<uint4*>(sPg + sw_off(r, (c0 >> 3) + u, kT)) =
-                            make_uint4(pkd[4 * u], pkd[4 * u + 1], pkd[4 * u + 2], pkd[4 * u + 3]);
-                }
-                l = l * alpha + sum;
-                mref = mnew;
-                const bool resc = c > 0 && alpha != 1.0f;
-                if (__any_sync(0xffffffffu, resc)) {
-                    // O holds the previous chunk's O += P V once that MMA is done; S(g)
-                    // complete implies every MMA before it, PV(g-2) included, is done, so
-                    // this wait can only see PV(g-1)'s phase
-                    if (!__all_sync(0xffffffffu, ws_wait(&pv_done, (g - 1) & 1, status, abort_v))) {
-                        ok = false;
-                        break;
-                    }
-                    fence_after_sync();
-#pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        float o[32];
-                        tmem_ld32(tO + c0, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] *= alpha;
-                        tmem_st32(tO + c0, o);
-                    }
-                    tmem_wait_st();
-                }
-                fence_proxy_async();
-                fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[g & 1]);
-            }
-            if (!ok) break;
-            // epilogue: normalized partial (or output) of each valid row
-            if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (tseq >> 1) & 1, status, abort_v))) break;
-            fence_after_sync();
-            const uint32_t tO = lane_base(tmem) + kO0 + ob * 128;
-            const bool valid = q >= 0;
-            const int bh = ti.bh;
-            const float inv = valid ? 1.0f / l : 0.0f;
-            const size_t pr = valid ? ((size_t)bh * N + q) * s + slot : 0;
-            __nv_bfloat16* dst = !valid ? nullptr : (s == 1) ? O + ((size_t)bh * N + q) * D : part + pr * D;
-            {
-                float o[D];
-#pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(tO + c0, o + c0);
-                tmem_wait_ld();
-                fence_before_sync();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&o_free[ob]);   // O is read: the tile after next may accumulate into it
-                    mbar_arrive(&q_empty[qs]);  // row list and query tile no longer needed
-                }
-                if (valid) {
-#pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 8)
-                        *reinterpret_cast<uint4*>(dst + c0) =
-                            make_uint4(pack_bf16(o[c0] * inv, o[c0 + 1] * inv), pack_bf16(o[c0 + 2] * inv, o[c0 + 3] * inv),
-                                       pack_bf16(o[c0 + 4] * inv, o[c0 + 5] * inv), pack_bf16(o[c0 + 6] * inv, o[c0 + 7] * inv));
-                }
-            }
-            if (valid && s > 1) merge_partials<D>(O, part, lse, cnt, bh, N, q, s, pr, mref + __log2f(l));
-            ++tseq;
-        }
-    }
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    if (warp == 4 + kNPW) tmem_dealloc(tmem, 512);
-}
+// Producer warps of the expert kernel.
+constexpr int kNPW = 3;
 
 // ------------------------------------------------------------------------
 // Expert attention with the expert's keys and values resident in shared
-// memory (k <= 256, m <= 128). Persistent, one CTA per SM. The CTAs claim
-// whole experts (all tiles of one (head, expert) bucket) from a counter, in
-// head order: the load stays balanced, an expert's keys and values are
-// gathered once for all its tiles, and at any moment all SMs work on about
-// one head. The shared slots come in as a separate partial (routing kernel);
-// the merge kernel combines the partials. The probabilities are written over
+// memory. Persistent, one CTA per SM. The CTAs claim whole experts (all
+// tiles of one (head, expert) bucket) from a counter, in head order: the load
+// stays balanced, an expert's keys and values are gathered once for all its
+// tiles, and at any moment all SMs work on about one head. An expert of more
+// than 256 keys is cut into sub-experts of ksub <= 256 consecutive keys of its
+// (ascending) set, each its own work unit with its own partial output; the
+// merge kernel combines every partial of a query by log-sum-exp, which is the
+// softmax over the union of their keys. The probabilities are written over
 // the scores in TMEM and O += P V reads them from there.
+//
+// Shared mode (I == nullptr): the same kernel computes the shared slots of
+// every query (keys Qt, values Vt: the bf16 rows K, V of each head, kv_head_rows
+// apart) over tiles of 128 consecutive queries, in claims of sh_grp tiles,
+// and with more than 256 landmarks in sub-experts as above.
 //
 // Chunk stream: chunk g is key chunk c = g % nex of the CTA's tile g / nex.
 // The MMA warp keeps S of chunks g and g + 1 in flight while the softmax
@@ -1675,19 +1327,26 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 // rows.
 struct ResTile {
     int bh, e, start, rows, gen;  // gen: loads of the resident keys so far (this tile uses load gen - 1); rows < 0: end
+    int sub, kk;                  // sub-expert and its key count
 };
 
 // expert attention with resident keys: warps 0-7 softmax + epilogue,
 // 8 .. 8 + kNPW - 1 producers, then the MMA warp
 constexpr int kResThreads = 32 * (8 + kNPW + 1);
+// The launch gives every thread 168 registers; the producer and MMA warpgroup
+// hands some down (kResRegsLo) and the two softmax warpgroups take them up
+// (kResRegsHi): 4 * 32 * Lo + 8 * 32 * Hi = 384 * 168.
+constexpr int kResRegsLo = 120, kResRegsHi = 192;
+static_assert(kResThreads == 384 && 4 * kResRegsLo + 8 * kResRegsHi == 12 * 168, "register split must match the launch");
 
 template <int D>
 __global__ void __launch_bounds__(kResThreads, 1)
     k_expert_res(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
-                 const __nv_bfloat16* __restrict__ V, const int32_t* __restrict__ I, const int32_t* __restrict__ perm,
-                 const int4* __restrict__ tiles, const int2* __restrict__ xtl, int nx, int* __restrict__ work_ctr,
-                 __nv_bfloat16* __restrict__ part, float* __restrict__ lse, int N, int m, int k, int s, float sl,
-                 int causal, int stall, int* __restrict__ status) {
+                 const __nv_bfloat16* __restrict__ V, long long kv_head_rows, const int32_t* __restrict__ I,
+                 const int32_t* __restrict__ perm, const int4* __restrict__ tiles, const int2* __restrict__ xtl,
+                 int nx, int* __restrict__ work_ctr, __nv_bfloat16* __restrict__ part, float* __restrict__ lse, int N,
+                 int m, int k, int s, int ksub, int nsub, int sh_tph, int sh_grp, float sl, int causal, int stall,
+                 int* __restrict__ status) {
     constexpr int TILE = kT * D * 2;
     constexpr uint32_t kS0 = 0, kO0 = 256;  // TMEM: S/P buffers 0 / 128, O buffers 256 / 384
     extern __shared__ uint8_t smem_raw[];
@@ -1714,7 +1373,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
     const long long lim = stall ? kSpinTest : kSpin;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nex = (k + kT - 1) / kT;  // <= 2
+    const int nex = (ksub + kT - 1) / kT;  // <= 2
     if (warp == 8 + kNPW) tmem_alloc(&tmem_slot, 512);
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -1744,6 +1403,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
 
     if (warp >= 8 && warp < 8 + kNPW) {
         // ------------------------------------------------------- producers
+        regs_dec<kResRegsLo>();
         // Warp 0 claims the work and hands each tile to all producer warps
         // (named barrier 1); all kNPW warps gather the tile's query rows and
         // the resident keys / values (row pairs dealt round-robin). The index
@@ -1751,11 +1411,13 @@ __global__ void __launch_bounds__(kResThreads, 1)
         // indices when the expert changes) are issued one tile ahead, so that
         // no gather waits on a dependent global load.
         const int pw = warp - 8;
-        int cur_bh = -1, cur_e = -1, gen = 0;
+        int cur_bh = -1, cur_e = -1, cur_u = -1, gen = 0;
         int x_t = 0, x_end = 0;         // warp 0, lane 0: tiles left of the claimed expert
+        int x_u = 0, x_bh = 0;          // warp 0, lane 0: its sub-expert (and head, shared mode)
         bool stall_pending = false;     // fault test: this CTA's first tile goes unpublished
         const int cc = lane % CPR;
-        // warp 0, lane 0: the next tile of the claimed work (w < 0: none left)
+        // warp 0, lane 0: the next tile of the claimed work (w < 0: none left);
+        // w = rows | (sub-expert << 16)
         auto next_tile = [&]() -> int4 {
             int4 td = make_int4(0, 0, 0, -1);
             if (*abort_v) return td;
@@ -1763,32 +1425,50 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 const int x = atomicAdd(work_ctr, 1);
                 if (x >= nx) return td;
                 if (x == 0 && stall) stall_pending = true;
-                const int2 r = xtl[x];
-                x_t = r.x;
-                x_end = r.x + r.y;
+                if (I) {  // expert x / nsub, sub-expert x % nsub
+                    const int2 r = xtl[x / nsub];
+                    x_t = r.x;
+                    x_end = r.x + r.y;
+                    x_u = x % nsub;
+                } else {  // head, sub-expert, group of sh_grp query tiles
+                    const int ngrp = (sh_tph + sh_grp - 1) / sh_grp;
+                    x_bh = x / (nsub * ngrp);
+                    x_u = (x / ngrp) % nsub;
+                    x_t = (x % ngrp) * sh_grp;
+                    x_end = min(sh_tph, x_t + sh_grp);
+                }
             }
-            return tiles[x_t++];
+            if (I) {
+                int4 t = tiles[x_t++];
+                t.w = (t.w & 255) | (x_u << 16);
+                return t;
+            }
+            const int start = (x_t++) * kT;
+            return make_int4(x_bh, 0, start, min(kT, N - start) | (x_u << 16));
         };
+        // keys of sub-expert u
+        auto keys_of = [&](int u) { return min(ksub, k - u * ksub); };
         // this lane's rows of a tile: r = lane + 32 i, the ones dealt to this warp
         auto own = [&](int r) { return ((r / RPI) % kNPW) == pw; };
         int pkv[kT / 32];        // bucket entries (q << 3 | slot) of the next tile's rows, -1 for none
         int krv[2][kT / 32];     // key indices of the next expert's rows (when it changes)
         auto prefetch = [&](const int4& td) {
-            const int rows = td.w & 255;
-            const int32_t* pb = perm + (size_t)td.x * N * s + td.z;
+            const int rows = td.w & 255, u = td.w >> 16;
+            const int32_t* pb = I ? perm + (size_t)td.x * N * s + td.z : nullptr;
 #pragma unroll
             for (int i = 0; i < kT / 32; ++i) {
                 const int r = lane + 32 * i;
-                pkv[i] = (td.w >= 0 && own(r) && r < rows) ? pb[r] : -1;
+                pkv[i] = (td.w >= 0 && own(r) && r < rows) ? (I ? pb[r] : (td.z + r) << 3) : -1;
             }
-            if (td.w >= 0 && (td.x != cur_bh || td.y != cur_e)) {
-                const int32_t* Ie = I + ((size_t)td.x * m + td.y) * k;
+            if (td.w >= 0 && (td.x != cur_bh || td.y != cur_e || u != cur_u)) {
+                const int kk = keys_of(u);
+                const int32_t* Ie = I ? I + ((size_t)td.x * m + td.y) * k + (size_t)u * ksub : nullptr;
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
 #pragma unroll
                     for (int i = 0; i < kT / 32; ++i) {
                         const int t2 = c * kT + lane + 32 * i;
-                        krv[c][i] = (c < nex && own(lane + 32 * i) && t2 < k) ? Ie[t2] : 0;
+                        krv[c][i] = (c < nex && own(lane + 32 * i) && t2 < kk) ? (I ? Ie[t2] : u * ksub + t2) : 0;
                     }
             }
         };
@@ -1805,14 +1485,14 @@ __global__ void __launch_bounds__(kResThreads, 1)
             if (pstop) break;
             if (td.w < 0) {
                 // no more work: an end marker for the consumers, in the free slot
-                if (pw == 0 && lane == 0) tinfo[qs] = ResTile{0, 0, 0, -1, 0};
+                if (pw == 0 && lane == 0) tinfo[qs] = ResTile{0, 0, 0, -1, 0, 0, 0};
                 cp_async_arrive(&q_full[qs]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&q_full[qs]);
                 break;
             }
-            const int bh = td.x, e = td.y, start = td.z, rows = td.w & 255;
-            const bool reload = bh != cur_bh || e != cur_e;
+            const int bh = td.x, e = td.y, start = td.z, rows = td.w & 255, u = td.w >> 16, kk = keys_of(u);
+            const bool reload = bh != cur_bh || e != cur_e || u != cur_u;
             (void)start;
 #pragma unroll
             for (int i = 0; i < kT / 32; ++i) {
@@ -1833,7 +1513,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                     for (int c = 0; c < 2; ++c)
 #pragma unroll
                         for (int i = 0; i < kT / 32; ++i)
-                            if (own(lane + 32 * i) && c * kT + lane + 32 * i < k)
+                            if (own(lane + 32 * i) && c * kT + lane + 32 * i < kk)
                                 keyall[c * kT + lane + 32 * i] = krv[c][i];
                     named_sync(1, 32 * kNPW);
                 }
@@ -1842,7 +1522,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                     const int r = lane + 32 * i;
                     if (!own(r)) continue;
                     const int pk = rowq[qs][r];
-                    int lo = 0, hi = k;  // first index with key > q
+                    int lo = 0, hi = kk;  // first index with key > q
                     if (pk >= 0) {
                         const int q = pk >> 3;
                         while (lo < hi) {
@@ -1854,7 +1534,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                     rowok[qs][r] = lo;
                 }
             }
-            if (pw == 0 && lane == 0) tinfo[qs] = ResTile{bh, e, start, rows, gen + (reload ? 1 : 0)};
+            if (pw == 0 && lane == 0) tinfo[qs] = ResTile{bh, e, start, rows, gen + (reload ? 1 : 0), u, kk};
             __syncwarp();
             {
                 const __nv_bfloat16* Qb = Q + (size_t)bh * N * D;
@@ -1873,8 +1553,8 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 if (lane == 0 && !skip) mbar_arrive(&q_full[qs]);
             }
             if (reload) {
-                const __nv_bfloat16* Kb = K + (size_t)bh * N * D;
-                const __nv_bfloat16* Vb = V + (size_t)bh * N * D;
+                const __nv_bfloat16* Kb = K + (size_t)bh * kv_head_rows * D;
+                const __nv_bfloat16* Vb = V + (size_t)bh * kv_head_rows * D;
                 bool okc = true;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {  // nex <= 2 chunks (unrolled: krv stays in registers)
@@ -1891,7 +1571,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                         const int r = lane + 32 * i;
                         if (!own(r)) continue;
                         int j = krv[c][i];
-                        if (j < 0 || j >= N) {
+                        if (j < 0 || j >= kv_head_rows) {
                             set_status(status, kStBounds);
                             j = 0;
                         }
@@ -1915,6 +1595,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
                     ++gen;
                     cur_bh = bh;
                     cur_e = e;
+                    cur_u = u;
                 }
             }
             // the next tile, and its index loads in flight while this one is consumed
@@ -1926,6 +1607,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
         cp_async_wait_all();  // nothing of ours may still be in flight when the CTA exits
     } else if (warp == 8 + kNPW) {
         // ------------------------------------------------------ MMA issuer
+        regs_dec<kResRegsLo>();
         // One thread polls the barriers without blocking: O += P V of chunk g
         // goes out as soon as its probabilities are in, and S of the next
         // chunk as soon as its query tile and keys are; neither waits behind
@@ -2022,6 +1704,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
         __syncwarp();
     } else {
         // -------------------------------------------- softmax + epilogue
+        regs_inc<kResRegsHi>();
         // two warpgroups share each row: wg 0 takes keys 0..63 of a chunk and
         // output columns 0..D/2-1, wg 1 the other halves; the row max and the
         // row sum are exchanged through shared memory (bounded mbarrier waits)
@@ -2059,7 +1742,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
             }
             if (lane == 0) mbar_arrive(&o_free[ob]);
             const float inv = (pk >= 0 && lt > 0.0f) ? 1.0f / lt : 0.0f;  // no key (causal only): zero partial
-            const size_t pr = pk >= 0 ? ((size_t)pti.bh * N + (pk >> 3)) * s + (pk & 7) : 0;
+            const size_t pr = pk >= 0 ? (((size_t)pti.bh * N + (pk >> 3)) * s + (pk & 7)) * nsub + pti.sub : 0;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // lanes 16h .. 16h + 15 stage their rows
                 if ((lane >> 4) == h) {
@@ -2100,7 +1783,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
             const ResTile ti = tinfo[qs];
             if (ti.rows < 0) break;  // end of the work
             const int pk = rowq[qs][r];
-            const int kok = causal ? rowok[qs][r] : k;  // the row's keys (a prefix of the expert's)
+            const int kok = causal ? rowok[qs][r] : ti.kk;  // the row's keys (a prefix of the sub-expert's)
             __syncwarp();
             if (lane == 0) mbar_arrive(&q_empty[qs]);  // tinfo / rowq read; the MMA releases the tile itself
             const bool valid = pk >= 0;
@@ -2250,6 +1933,12 @@ TcPlan tc_plan(const Dims& D) {
     p.n_samp = (int)(((long long)D.N + 16LL * R - 1) / (16LL * R) * 16);
     p.cand_cap = (long long)p.chunks_per_split * kT;
     p.resident = D.shared && p.m_pad == kT && D.k <= 2 * kT;
+    p.route_shared = D.shared && p.m_pad == kT;
+    p.ksub = std::min(D.k, 2 * kT);
+    p.nsub = (D.k + p.ksub - 1) / p.ksub;
+    p.ksub_sh = std::min(D.m, 2 * kT);
+    p.nsub_sh = (D.m + p.ksub_sh - 1) / p.ksub_sh;
+    p.nsh = !D.shared ? 0 : p.route_shared ? 1 : p.nsub_sh;
     return p;
 }
 
@@ -2299,7 +1988,7 @@ static cudaError_t launch_route_s(const Dims& D, const TcPlan& P, const TcWork& 
                                   int32_t* E, int* status, cudaStream_t st) {
     cudaError_t e;
     const int tile = kT * DD * 2;
-    if (P.resident) {  // routes + the shared-slot partial in one pass
+    if (P.route_shared) {  // routes + the shared-slot partial in one pass
         alignas(64) CUtensorMap mq;
         if ((e = tile_map(&mq, q, (long long)D.BH * D.N, DD))) return e;
         constexpr int NSQ = 3;
@@ -2413,30 +2102,38 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
         if ((e = cudaGetLastError())) return e;
         count_launch(3);
     }
-    // expert attention + merge
+    // expert attention (and, with more than 128 landmarks, the shared slots) + merge
     {
-        if (P.resident) {
-            prof_mark(st, "expert_res");
-            const int smem = 6 * tile + 8 * kStageWarp + 1024;
-            if ((e = set_smem(k_expert_res<DD>, smem))) return e;
+        const int smem = 6 * tile + 8 * kStageWarp + 1024;
+        const int stall = (D.flags & MITA_TESTFLAG_STALL_PRODUCER) ? 1 : 0;
+        if ((e = set_smem(k_expert_res<DD>, smem))) return e;
+        if (P.nsh && !P.route_shared) {
+            prof_mark(st, "shared");
+            const int tph = (D.N + kT - 1) / kT;
+            const long long want = (long long)D.BH * P.nsub_sh * tph / (8LL * num_sms());
+            const int grp = (int)std::max(1LL, std::min((long long)tph, want));
+            const int ngrp = (tph + grp - 1) / grp;
             k_expert_res<DD><<<num_sms(), kResThreads, smem, st>>>(
-                q, kk, v, I, W.perm, W.tiles, W.xtl, D.BH * D.m, W.tile_ctr + 1, W.part, W.lse, D.N, D.m, D.k, D.s,
-                sl, D.causal ? 1 : 0, (D.flags & MITA_TESTFLAG_STALL_PRODUCER) ? 1 : 0, status);
+                q, W.Qhi, W.Vtb, P.m_pad, nullptr, nullptr, nullptr, nullptr, D.BH * P.nsub_sh * ngrp, W.tile_ctr + 2,
+                W.sh_part, W.sh_lse, D.N, D.m, D.m, 1, P.ksub_sh, P.nsub_sh, tph, grp, sl, 0, stall, status);
             if ((e = cudaGetLastError())) return e;
             count_launch();
-            prof_mark(st, "merge");
-            const long long nq = (long long)D.BH * D.N;
-            k_merge<DD><<<(unsigned)((nq * (DD / 8) + 255) / 256), 256, 0, st>>>(W.part, W.lse, W.sh_part, W.sh_lse,
-                                                                               (__nv_bfloat16*)O, nq, D.s);
-        } else {
-            prof_mark(st, "expert_ws");
-            const int smem = 4 * tile + 2 * kp_bytes<DD>() + 1024;
-            if ((e = set_smem(k_expert_ws<DD>, smem))) return e;
-            k_expert_ws<DD><<<num_sms(), kWsThreads, smem, st>>>(q, kk, v, W.Qhi, W.Vtb, I, W.perm, W.tiles,
-                                                                 W.tile_ctr, (__nv_bfloat16*)O, W.part, W.lse, W.cnt,
-                                                                 D.N, D.m, P.m_pad, D.k, D.s, D.shared ? 1 : 0, sl,
-                                                                 status);
         }
+        prof_mark(st, "expert_res");
+        k_expert_res<DD><<<num_sms(), kResThreads, smem, st>>>(
+            q, kk, v, D.N, I, W.perm, W.tiles, W.xtl, D.BH * D.m * P.nsub, W.tile_ctr + 1, W.part, W.lse, D.N, D.m,
+            D.k, D.s, P.ksub, P.nsub, 0, 1, sl, D.causal ? 1 : 0, stall, status);
+        if ((e = cudaGetLastError())) return e;
+        count_launch();
+        prof_mark(st, "merge");
+        const long long nq = (long long)D.BH * D.N;
+        const unsigned mblocks = (unsigned)((nq * (DD / 8) + 255) / 256);
+        if (D.s * P.nsub <= kMaxS && P.nsh <= 1)
+            k_merge_few<DD><<<mblocks, 256, 0, st>>>(W.part, W.lse, P.nsh ? W.sh_part : nullptr, W.sh_lse,
+                                                     (__nv_bfloat16*)O, nq, D.s * P.nsub);
+        else
+            k_merge<DD><<<mblocks, 256, 0, st>>>(W.part, W.lse, D.s * P.nsub, W.sh_part, W.sh_lse, P.nsh,
+                                                 (__nv_bfloat16*)O, nq);
         if ((e = cudaGetLastError())) return e;
         count_launch();
     }
