@@ -55,11 +55,11 @@ def work_counts(w):
     return F, Bytes
 
 
-def expert_flops(w, with_shared):
+def expert_flops(w):
     """Algorithmic flops of one expert-attention launch: q . k and p . v over
-    the s * k routed slots of every query (plus the m shared slots when the
-    kernel computes those too)."""
-    return 4.0 * w.BH * w.N * w.d * (w.s * w.k + (w.m if with_shared else 0))
+    the s * k routed slots of every query (the shared slots run in the routing
+    pass, or with more than 128 landmarks in a pass of their own)."""
+    return 4.0 * w.BH * w.N * w.d * w.s * w.k
 
 
 def tc_cu_sha16():
@@ -257,12 +257,11 @@ def expert_roofline(w, phase_ms, pk, pk_src, ms_step):
     launching stream around the launch, inside the timed region), against the
     measured burst bf16 peak (the step is milliseconds long, not a sustained
     seconds-long loop); the sustained peak is given beside it."""
-    phase = next(k for k in phase_ms if k.startswith("expert"))
-    resident = phase == "expert_res"  # k_expert_res; the shared slots ran in the routing pass
-    flops = expert_flops(w, with_shared=not resident)
+    phase = "expert_res"
+    flops = expert_flops(w)
     ms = phase_ms[phase]
     achieved = flops / (ms * 1e-3) / 1e12
-    kernel = "k_expert_res" if resident else "k_expert_ws"
+    kernel = "k_expert_res"
     traffic = None
     if EXPERT_TRAFFIC["kernel"] == kernel and EXPERT_TRAFFIC["tc_cu_sha16"] == tc_cu_sha16() \
             and w.name == "longctx_n32k":
@@ -275,7 +274,7 @@ def expert_roofline(w, phase_ms, pk, pk_src, ms_step):
             "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % pk_src,
             "frac_of_sustained": achieved / sus if sus else None,
             "algorithmic_flops_per_launch": flops,
-            "flops_counted": "4*B*H*N*d*s*k (routed slots)" if resident else "4*B*H*N*d*(s*k+m) (routed + shared slots)",
+            "flops_counted": "4*B*H*N*d*s*k (routed slots)",
             "avg_launch_ms": ms, "share_of_step": ms / ms_step}
 
 
@@ -380,7 +379,7 @@ def main():
                        "path": "tcgen05" if uses_tc else "cuda-core", "l2": "inputs larger than L2 (no flush)",
                        "parallelism": "replicas x%d" % world},
             "roofline": expert_roofline(w, phase_ms, pk, pk_src, ms_step)
-            if any(k.startswith("expert") for k in phase_ms) else None,
+            if "expert_res" in phase_ms else None,
             "path_roofline": {"t_roof_us": t_roof * 1e6, "frac": t_roof / (ms_step * 1e-3),
                               "flops": F, "compulsory_bytes": Bytes,
                               "peaks": {"bf16_tflops": pk["bf16_tflops"], "hbm_gbs": pk["hbm_gbs"],

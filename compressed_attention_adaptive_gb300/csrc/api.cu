@@ -170,7 +170,6 @@ static Work carve(const Dims& D, void* ws, size_t* bytes) {
         t.perm = c.take<int32_t>(BH * D.N * D.s);
         t.part = c.take<__nv_bfloat16>(BH * D.N * D.s * P.nsub * D.d);
         t.lse = c.take<float>(BH * D.N * D.s * P.nsub);
-        t.cnt = c.take<int>(BH * D.N);
         if (P.nsh) {
             t.sh_part = c.take<__nv_bfloat16>(BH * D.N * P.nsh * D.d);
             t.sh_lse = c.take<float>(BH * D.N * P.nsh);

@@ -89,7 +89,6 @@ struct TcWork {
     int32_t* perm;                   // [BH][N*s]
     __nv_bfloat16* part;             // [BH][N][s][nsub][d]
     float* lse;                      // [BH][N][s][nsub]
-    int* cnt;                        // [BH][N]
     __nv_bfloat16* sh_part;          // [BH][N][nsh][d] shared-slot partials
     float* sh_lse;                   // [BH][N][nsh]
 };

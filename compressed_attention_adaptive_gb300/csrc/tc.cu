@@ -161,16 +161,24 @@ __device__ __forceinline__ void emit_cand(int2* base, int& n, float score, int k
     n += pass ? 1 : 0;
 }
 
-// Largest of 64 values (a tree: six levels of independent maxima).
+// Largest of three (the three-input max.f32 of sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Largest of 64 values: a tree of three-input maxima (four levels).
 __device__ __forceinline__ float max64(const float (&v)[64]) {
-    float t[32];
+    float t[22];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) t[j] = fmaxf(v[2 * j], v[2 * j + 1]);
+    for (int j = 0; j < 21; ++j) t[j] = fmax3(v[3 * j], v[3 * j + 1], v[3 * j + 2]);
+    t[21] = v[63];
+    float u[8];
 #pragma unroll
-    for (int h = 16; h >= 1; h >>= 1)
-#pragma unroll
-        for (int j = 0; j < h; ++j) t[j] = fmaxf(t[j], t[j + h]);
-    return t[0];
+    for (int j = 0; j < 7; ++j) u[j] = fmax3(t[3 * j], t[3 * j + 1], t[3 * j + 2]);
+    u[7] = t[21];
+    return fmax3(fmax3(u[0], u[1], u[2]), fmax3(u[3], u[4], u[5]), fmaxf(u[6], u[7]));
 }
 
 // Lowest j with v[j] == x, 64 if there is none (a tree of minima).
@@ -564,12 +572,10 @@ __global__ void k_vt_combine(const float* __restrict__ Opart, const float2* __re
 // ------------------------------------------------------------------------
 // Routing: R = Q Qhi^T + Q Qlo^T (the bf16 split of fp32 Qt keeps routing
 // scores at fp32 accuracy), then each thread keeps the s best landmarks of
-// its query row (ties to the lower landmark index). Also clears the
-// per-query merge counters.
+// its query row (ties to the lower landmark index).
 
 template <int SMAX>
-__device__ __forceinline__ void route_epilogue(uint32_t tR, int m, int s, int q, bool q_ok, int32_t* __restrict__ Erow,
-                                               int* __restrict__ cnt_q) {
+__device__ __forceinline__ void route_epilogue(uint32_t tR, int m, int s, int q, bool q_ok, int32_t* __restrict__ Erow) {
     // the SMAX best landmarks so far (s <= SMAX of them are written), descending,
     // ties to the lower index; blocks of 64 are visited in increasing index order,
     // and a block only contributes while its largest remaining score beats the
@@ -601,7 +607,6 @@ __device__ __forceinline__ void route_epilogue(uint32_t tR, int m, int s, int q,
 #pragma unroll
         for (int t = 0; t < SMAX; ++t)
             if (t < s) Erow[t] = bi[t];
-        *cnt_q = 0;
     }
 }
 
@@ -613,7 +618,7 @@ template <int D, int SMAX>
 __global__ void __launch_bounds__(128, 1)
     k_route_tc(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Qhi,
                const __nv_bfloat16* __restrict__ Qlo, int N, int m, int m_pad, int s, int tiles_per_head,
-               int total_tiles, uint32_t tmem_cols, int32_t* __restrict__ E, int* __restrict__ cnt,
+               int total_tiles, uint32_t tmem_cols, int32_t* __restrict__ E,
                int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar;
@@ -701,8 +706,7 @@ __global__ void __launch_bounds__(128, 1)
         }
         const int bh = t / tiles_per_head, q = (t % tiles_per_head) * kT + r;
         const bool q_ok = q < N;
-        route_epilogue<SMAX>(lane_base(tmem) + b * m_pad, m, s, q, q_ok, E + ((size_t)bh * N + (q_ok ? q : 0)) * s,
-                             cnt + (size_t)bh * N + (q_ok ? q : 0));
+        route_epilogue<SMAX>(lane_base(tmem) + b * m_pad, m, s, q, q_ok, E + ((size_t)bh * N + (q_ok ? q : 0)) * s);
         fence_before_sync();
     }
     // drain an MMA still in flight if the loop left early
@@ -1011,7 +1015,7 @@ template <int D, int SMAX>
 __global__ void __launch_bounds__(128)
     k_route_chunked_tc(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Qhi,
                        const __nv_bfloat16* __restrict__ Qlo, int N, int m, int m_pad, int s, uint32_t tmem_cols,
-                       int32_t* __restrict__ E, int* __restrict__ cnt, int* __restrict__ status) {
+                       int32_t* __restrict__ E, int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar;
     __shared__ uint32_t tmem_slot;
@@ -1054,8 +1058,7 @@ __global__ void __launch_bounds__(128)
     if (ok) {
         const int q = q0 + r;
         const bool q_ok = q < N;
-        route_epilogue<SMAX>(tR, m, s, q, q_ok, E + ((size_t)bh * N + (q_ok ? q : 0)) * s,
-                             cnt + (size_t)bh * N + (q_ok ? q : 0));
+        route_epilogue<SMAX>(tR, m, s, q, q_ok, E + ((size_t)bh * N + (q_ok ? q : 0)) * s);
     }
     fence_before_sync();
     __syncthreads();
@@ -1065,13 +1068,13 @@ __global__ void __launch_bounds__(128)
 
 // ------------------------------------------------------------------------
 // Bucketing of (query, slot) pairs by routed expert. Within an expert's
-// bucket the slot-0 pairs come first (they also attend to the shared slots),
-// then the others; each bucket is cut into 128-row work tiles.
+// bucket the slot-0 pairs come first, then the others (a fixed order, so the
+// work tiles are the same from run to run); each bucket is cut into 128-row
+// work tiles.
 
 // counts[bh][e][cls], cls = 0 for slot 0, 1 for slots >= 1.
-// Also clears the per-query merge counters of the expert attention.
 __global__ void k_bucket_count(const int32_t* __restrict__ E, int N, int m, int s, int* __restrict__ counts,
-                               int use_smem, int* __restrict__ cnt, int* __restrict__ status) {
+                               int use_smem, int* __restrict__ status) {
     extern __shared__ int hist[];
     const int bh = blockIdx.y;
     if (use_smem) {
@@ -1080,7 +1083,6 @@ __global__ void k_bucket_count(const int32_t* __restrict__ E, int N, int m, int 
     }
     const int q = blockIdx.x * blockDim.x + threadIdx.x;
     if (q < N) {
-        cnt[(size_t)bh * N + q] = 0;
         for (int t = 0; t < s; ++t) {
             const int e = E[((size_t)bh * N + q) * s + t];
             if (e < 0 || e >= m) {
@@ -1100,7 +1102,7 @@ __global__ void k_bucket_count(const int32_t* __restrict__ E, int N, int m, int 
 }
 
 // Per head: bucket offsets, scatter cursors and the head's work tiles
-// (x = head, y = expert, z = first bucket row, w = rows | shared_rows << 8).
+// (x = head, y = expert, z = first bucket row, w = rows | slot_0_rows << 8).
 // xtl[bh * m + e] = (first tile, tile count) of each expert's bucket.
 __global__ void __launch_bounds__(512) k_bucket_scan(const int* __restrict__ counts, int m, int Ns,
                                                      int* __restrict__ cursors, int* __restrict__ toff,
@@ -2007,13 +2009,13 @@ static cudaError_t launch_route_s(const Dims& D, const TcPlan& P, const TcWork& 
         const int total = tph * D.BH;
         const int grid = std::min(total, num_sms());
         k_route_tc<DD, SMAX><<<grid, 128, smem, st>>>(q, W.Qhi, W.Qlo, D.N, D.m, P.m_pad, D.s, tph, total,
-                                                      (uint32_t)P.route_cols, E, W.cnt, status);
+                                                      (uint32_t)P.route_cols, E, status);
     } else {
         const int smem = std::max(3 * tile, 100 * 1024) + 1024;
         if ((e = set_smem(k_route_chunked_tc<DD, SMAX>, smem))) return e;
         dim3 grid((D.N + kT - 1) / kT, D.BH);
         k_route_chunked_tc<DD, SMAX><<<grid, 128, smem, st>>>(q, W.Qhi, W.Qlo, D.N, D.m, P.m_pad, D.s,
-                                                              (uint32_t)P.route_cols, E, W.cnt, status);
+                                                              (uint32_t)P.route_cols, E, status);
     }
     if ((e = cudaGetLastError())) return e;
     count_launch();
@@ -2094,8 +2096,7 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
     {
         const int use_smem = D.m <= 4096;
         dim3 grid((D.N + 255) / 256, D.BH);
-        k_bucket_count<<<grid, 256, use_smem ? 8 * D.m : 0, st>>>(E, D.N, D.m, D.s, W.counts, use_smem, W.cnt,
-                                                                  status);
+        k_bucket_count<<<grid, 256, use_smem ? 8 * D.m : 0, st>>>(E, D.N, D.m, D.s, W.counts, use_smem, status);
         k_bucket_scan<<<D.BH, 512, 0, st>>>(W.counts, D.m, D.N * D.s, W.cursors, W.toff, W.tile_ctr, W.tiles,
                                             W.xtl);
         k_bucket_scatter<<<grid, 256, use_smem ? 8 * D.m : 0, st>>>(E, D.N, D.m, D.s, W.cursors, W.perm, use_smem);

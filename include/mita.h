@@ -218,10 +218,12 @@ mita_status mita_forward_static(const mita_params* p, const void* Q, const void*
 long long mita_launch_count(void);
 
 /* Opens a phase profile: until mita_profile_end(), every call records a CUDA
- * event on its stream at the start of each phase (landmark pooling, landmark
- * pass, top-k selection, shared-expert combine, routing, bucketing, expert
- * attention) and at its end; up to max_marks events in total (created here,
- * kept for reuse). Process-wide; not for concurrent calls. */
+ * event on its stream at the start of each phase (landmark pooling, top-k
+ * sample and threshold, landmark pass, top-k selection, shared-expert combine,
+ * routing, bucketing, the shared slots' own pass when there are more than 128
+ * landmarks, expert attention, merge) and at its end; up to max_marks events
+ * in total (created here, kept for reuse). Process-wide; not for concurrent
+ * calls. */
 mita_status mita_profile_begin(int max_marks);
 
 /* Closes the profile: waits for the last event, sums the milliseconds of each

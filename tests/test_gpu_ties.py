@@ -33,7 +33,7 @@ TIES = [
     W("resident_zero_band", N=1024, m=16, k=256, s=2, zero_frac=0.6),  # the k-th score is 0 in half the rows
     W("resident", N=4096, m=32, k=256, s=2),
     W("resident_d64", N=2048, d=64, m=16, k=128, s=3, zero_frac=0.3),
-    W("streaming_zero_band", N=4096, m=64, k=1024, s=3, zero_frac=0.4),
+    W("sub_experts_zero_band", N=4096, m=64, k=1024, s=3, zero_frac=0.4),  # four 256-key sub-experts
     W("route_m256", N=4096, m=256, k=128, s=8, zero_frac=0.2),
     W("route_chunked_m512", N=8192, m=512, k=64, s=4, k_centers=4, zero_frac=0.0),
     W("all_rows_equal", N=2048, m=16, k=100, s=2, k_centers=1, zero_frac=0.0),
