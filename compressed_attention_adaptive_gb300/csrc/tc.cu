@@ -448,6 +448,7 @@ __global__ void __launch_bounds__(320, 1)
         float mref = -INFINITY, l = 0.0f;
         bool ok = true;
         const uint32_t tO = lane_base(tmem) + kO + wg * DH;
+        const bool warp_rows = __any_sync(0xffffffffu, row_ok);  // this warp holds a real landmark row
         for (int c = 0; c < nc; ++c) {
             const int sb = c & 1, j0 = j_begin + c * kT;
             if (!__all_sync(0xffffffffu, ws_wait(&s_full[sb], (c >> 1) & 1, status, abort_v, lim))) { ok = false; break; }
@@ -460,7 +461,9 @@ __global__ void __launch_bounds__(320, 1)
             tmem_ld32(tS + 64 * wg + 32, v + 32);
             tmem_wait_ld();
             float mx = -INFINITY;
-            if (nsm >= 64 && sl > 0.0f) {  // every column real: one tree maximum
+            if (!warp_rows) {
+                // padding rows only (m not a multiple of 128): nothing to emit or weigh
+            } else if (nsm >= 64 && sl > 0.0f) {  // every column real: one tree maximum
 #pragma unroll
                 for (int j = 0; j < 64; ++j) emit_cand(cw, ncand, v[j], j0 + 64 * wg + j, v[j] >= th);
                 mx = max64(v) * sl;
@@ -485,12 +488,17 @@ __global__ void __launch_bounds__(320, 1)
             }
             float sum = 0.0f;
             uint32_t pkd[32];
+            if (warp_rows) {
 #pragma unroll
-            for (int j = 0; j < 64; j += 2) {
-                const float e0 = ex2(fmaf(v[j], sl, -mnew)), e1 = ex2(fmaf(v[j + 1], sl, -mnew));
-                const float p0 = j < nsm ? e0 : 0.0f, p1 = j + 1 < nsm ? e1 : 0.0f;
-                sum += p0 + p1;
-                pkd[j >> 1] = pack_bf16(p0, p1);
+                for (int j = 0; j < 64; j += 2) {
+                    const float e0 = ex2(fmaf(v[j], sl, -mnew)), e1 = ex2(fmaf(v[j + 1], sl, -mnew));
+                    const float p0 = j < nsm ? e0 : 0.0f, p1 = j + 1 < nsm ? e1 : 0.0f;
+                    sum += p0 + p1;
+                    pkd[j >> 1] = pack_bf16(p0, p1);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) pkd[j] = 0u;
             }
             tmem_st32(tS + 32 * wg, reinterpret_cast<const float*>(pkd));
             tmem_wait_st();
@@ -959,12 +967,17 @@ __global__ void __launch_bounds__(320, 1)
             mx = fmaxf(mx, xmax[tl & 1][wg ^ 1][r]);
             float lsum = 0.0f;
             uint32_t pkd[32];
+            if (nval > 0) {
 #pragma unroll
-            for (int j = 0; j < 64; j += 2) {
-                const float e0 = ex2(fmaf(v[j], sl, -mx)), e1 = ex2(fmaf(v[j + 1], sl, -mx));
-                const float p0 = j < nsm ? e0 : 0.0f, p1 = j + 1 < nsm ? e1 : 0.0f;
-                lsum += p0 + p1;
-                pkd[j >> 1] = pack_bf16(p0, p1);
+                for (int j = 0; j < 64; j += 2) {
+                    const float e0 = ex2(fmaf(v[j], sl, -mx)), e1 = ex2(fmaf(v[j + 1], sl, -mx));
+                    const float p0 = j < nsm ? e0 : 0.0f, p1 = j + 1 < nsm ? e1 : 0.0f;
+                    lsum += p0 + p1;
+                    pkd[j >> 1] = pack_bf16(p0, p1);
+                }
+            } else {  // this half holds no landmark (m <= 64)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) pkd[j] = 0u;
             }
             tmem_st32(tR + 32 * wg, reinterpret_cast<const float*>(pkd));
             tmem_wait_st();
