@@ -582,18 +582,18 @@ __global__ void k_vt_combine(const float* __restrict__ Opart, const float2* __re
 // scores at fp32 accuracy), then each thread keeps the s best landmarks of
 // its query row (ties to the lower landmark index).
 
+// The SMAX best landmarks of columns [c_begin, c_end) (c_begin a multiple of
+// 64), descending, ties to the lower index; blocks of 64 are visited in
+// increasing index order, and a block only contributes while its largest
+// remaining score beats the SMAX-th best (an equal score has a higher index
+// and ranks behind). Empty entries: key 0, index -1.
 template <int SMAX>
-__device__ __forceinline__ void route_epilogue(uint32_t tR, int m, int s, int q, bool q_ok, int32_t* __restrict__ Erow) {
-    // the SMAX best landmarks so far (s <= SMAX of them are written), descending,
-    // ties to the lower index; blocks of 64 are visited in increasing index order,
-    // and a block only contributes while its largest remaining score beats the
-    // SMAX-th best (an equal score has a higher index and ranks behind)
-    uint32_t bu[SMAX];
-    int bi[SMAX];
+__device__ __forceinline__ void route_top(uint32_t tR, int c_begin, int c_end, uint32_t (&bu)[SMAX], int (&bi)[SMAX]) {
 #pragma unroll
     for (int t = 0; t < SMAX; ++t) { bu[t] = 0u; bi[t] = -1; }
+    const int m = c_end;
 #pragma unroll 1
-    for (int c0 = 0; c0 < m; c0 += 64) {
+    for (int c0 = c_begin; c0 < c_end; c0 += 64) {
         float v[64];
         tmem_ld32(tR + c0, v);
         tmem_ld32(tR + c0 + 32, v + 32);
@@ -611,6 +611,13 @@ __device__ __forceinline__ void route_epilogue(uint32_t tR, int m, int s, int q,
             mx = max64(v);
         }
     }
+}
+
+template <int SMAX>
+__device__ __forceinline__ void route_epilogue(uint32_t tR, int m, int s, int q, bool q_ok, int32_t* __restrict__ Erow) {
+    uint32_t bu[SMAX];
+    int bi[SMAX];
+    route_top<SMAX>(tR, 0, m, bu, bi);
     if (q_ok) {
 #pragma unroll
         for (int t = 0; t < SMAX; ++t)
@@ -621,9 +628,11 @@ __device__ __forceinline__ void route_epilogue(uint32_t tR, int m, int s, int q,
 // Persistent variant for m_pad <= 256: each CTA walks a contiguous range of
 // 128-query tiles; Qt (hi, lo) of the current head stays in shared memory and
 // the next query tile is loaded and multiplied while this tile's routes are
-// picked (two TMEM accumulators).
+// picked (two TMEM accumulators). Two warpgroups: each thread of warpgroup h
+// picks its query's best landmarks among the column blocks of half h, and
+// warpgroup 0 merges the two lists.
 template <int D, int SMAX>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
     k_route_tc(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Qhi,
                const __nv_bfloat16* __restrict__ Qlo, int N, int m, int m_pad, int s, int tiles_per_head,
                int total_tiles, uint32_t tmem_cols, int32_t* __restrict__ E,
@@ -631,17 +640,19 @@ __global__ void __launch_bounds__(128, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar;
     __shared__ uint32_t tmem_slot;
+    __shared__ uint32_t xkey[kT][SMAX];  // the second half's best, handed to the first
+    __shared__ int xidx[kT][SMAX];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int QT = m_pad * D * 2;
     uint8_t* sHi = sm;
     uint8_t* sLo = sm + QT;
     uint8_t* sQb[2] = {sm + 2 * QT, sm + 2 * QT + kT * D * 2};
-    const int r = threadIdx.x;
+    const int r = threadIdx.x & (kT - 1), half = threadIdx.x >> 7;
     const int per = (total_tiles + gridDim.x - 1) / gridDim.x;
     const int t_begin = blockIdx.x * per, t_end = min(total_tiles, t_begin + per);
     if (t_begin >= t_end) return;
-    if (r < 32) tmem_alloc(&tmem_slot, tmem_cols);
-    if (r == 0) {
+    if (threadIdx.x < 32) tmem_alloc(&tmem_slot, tmem_cols);
+    if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
         fence_mbar_init();
     }
@@ -689,7 +700,7 @@ __global__ void __launch_bounds__(128, 1)
     cp_async_wait_all();
     fence_proxy_async();
     __syncthreads();
-    if (r == 0) {
+    if (threadIdx.x == 0) {
         fence_after_sync();
         issue(0);
     }
@@ -707,21 +718,43 @@ __global__ void __launch_bounds__(128, 1)
             cp_async_wait_all();
             fence_proxy_async();
             __syncthreads();
-            if (r == 0) {
+            if (threadIdx.x == 0) {
                 fence_after_sync();
                 issue(b ^ 1);
             }
         }
         const int bh = t / tiles_per_head, q = (t % tiles_per_head) * kT + r;
         const bool q_ok = q < N;
-        route_epilogue<SMAX>(lane_base(tmem) + b * m_pad, m, s, q, q_ok, E + ((size_t)bh * N + (q_ok ? q : 0)) * s);
+        // column blocks of 64 split between the halves (the second half's blocks
+        // have the higher indices, so on equal scores the first half's win)
+        const int nblk = (m + 63) / 64, split = ((nblk + 1) / 2) * 64;
+        uint32_t bu[SMAX];
+        int bi[SMAX];
+        route_top<SMAX>(lane_base(tmem) + b * m_pad, half ? split : 0, half ? m : min(m, split), bu, bi);
+        if (half) {
+#pragma unroll
+            for (int u = 0; u < SMAX; ++u) {
+                xkey[r][u] = bu[u];
+                xidx[r][u] = bi[u];
+            }
+        }
         fence_before_sync();
+        __syncthreads();
+        if (!half && q_ok) {
+#pragma unroll
+            for (int u = 0; u < SMAX; ++u)
+                if (xidx[r][u] >= 0) top_insert<SMAX>(bu, bi, xkey[r][u], xidx[r][u]);
+            int32_t* Erow = E + ((size_t)bh * N + q) * s;
+#pragma unroll
+            for (int u = 0; u < SMAX; ++u)
+                if (u < s) Erow[u] = bi[u];
+        }
     }
     // drain an MMA still in flight if the loop left early
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (r < 32) tmem_dealloc(tmem, tmem_cols);
+    if (threadIdx.x < 32) tmem_dealloc(tmem, tmem_cols);
 }
 
 // Routing + shared slots, warp-specialized and persistent (m_pad == 128):
@@ -2021,7 +2054,7 @@ static cudaError_t launch_route_s(const Dims& D, const TcPlan& P, const TcWork& 
         const int tph = (D.N + kT - 1) / kT;
         const int total = tph * D.BH;
         const int grid = std::min(total, num_sms());
-        k_route_tc<DD, SMAX><<<grid, 128, smem, st>>>(q, W.Qhi, W.Qlo, D.N, D.m, P.m_pad, D.s, tph, total,
+        k_route_tc<DD, SMAX><<<grid, 256, smem, st>>>(q, W.Qhi, W.Qlo, D.N, D.m, P.m_pad, D.s, tph, total,
                                                       (uint32_t)P.route_cols, E, status);
     } else {
         const int smem = std::max(3 * tile, 100 * 1024) + 1024;
