@@ -17,6 +17,7 @@ region and rank 0 prints the job-wide line (max time over ranks).
 """
 import argparse
 import json
+import statistics
 import os
 import subprocess
 import sys
@@ -345,32 +346,40 @@ def main():
     torch.cuda.synchronize(dev)
     mita.mita_device_status(ws)
 
-    mita.mita_profile_begin(12 * args.steps + 16)
+    # The timed region replays one forward pass captured as a CUDA graph: all K
+    # steps are queued at once, so a stall of the host process cannot leave
+    # the GPU idle inside the region (eager launches can: the launch queue
+    # fills and the host then feeds it step by step).
+    graph, per_step_launches = capture_forward(mita, torch, p, Q, K, V, O, ws)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    mita.mita_device_status(ws)
     clocks = ClockSampler(local)
     time.sleep(0.3)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    n0 = mita.mita_launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        mita.mita_forward(p, Q, K, V, O, ws)
+        graph.replay()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
-    launches = mita.mita_launch_count() - n0
     clk = clocks.stop()
-    phases = mita.mita_profile_end()
     mita.mita_device_status(ws)
+    launches = per_step_launches * args.steps
     ms_step = job_max(dist, e0.elapsed_time(e1) / args.steps)
+    # phases (and the expert kernel's launch time for the roofline): a separate
+    # eager pass, one profile per step, median over the steps
+    phase_ms = profile_phases(mita, lambda: mita.mita_forward(p, Q, K, V, O, ws), min(args.steps, 30))
+    mita.mita_device_status(ws)
     value = world * w.BH * w.N / (ms_step * 1e-3)
 
     pk, pk_src = peaks()
     F, Bytes = work_counts(w)
     t_roof = max(F / (pk["bf16_tflops"] * 1e12), Bytes / (pk["hbm_gbs"] * 1e9))
-    phase_ms = {k: v / args.steps for k, v in phases.items()}
     uses_tc = mita.mita_uses_tensor_cores(p) == 1
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -384,7 +393,9 @@ def main():
                               "flops": F, "compulsory_bytes": Bytes,
                               "peaks": {"bf16_tflops": pk["bf16_tflops"], "hbm_gbs": pk["hbm_gbs"],
                                         "source": pk_src}},
-            "phases_ms": phase_ms, "gpu_launches": launches, "clocks": clk}
+            "phases_ms": phase_ms, "phases_how": "separate eager pass, median per phase over %d profiled steps"
+            % min(args.steps, 30), "timed_as": "one forward pass captured as a CUDA graph, replayed once per step",
+            "gpu_launches": launches, "clocks": clk}
 
     if not args.no_e2e:
         line["e2e"] = e2e_run(mita, p, Qn, Kn, Vn, w, dev, max(30, min(args.steps, 50)), dist, world)
@@ -395,8 +406,9 @@ def main():
 
 
 def sweep(args):
-    """Per configuration: step time (CUDA events over --steps steps after
-    --warmup), t_roof = max(F / bf16 peak, bytes / HBM peak) and their ratio."""
+    """Per configuration: step time (CUDA events over --steps replays of the
+    forward pass captured as a CUDA graph, after --warmup eager passes),
+    t_roof = max(F / bf16 peak, bytes / HBM peak) and their ratio."""
     import numpy as np
     import torch
     import compressed_attention_adaptive_gb300 as mita
@@ -413,18 +425,8 @@ def sweep(args):
         O = torch.empty_like(Q)
         p = mita.params_for(Q, w.m, w.k, w.s, w.grid, w.lm)
         ws = mita.workspace(p, dev)
-        stream = torch.cuda.current_stream(dev)
-        for _ in range(args.warmup):
-            mita.mita_forward(p, Q, K, V, O, ws)
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            mita.mita_forward(p, Q, K, V, O, ws)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
+        ms = _time_cuda(lambda: mita.mita_forward(p, Q, K, V, O, ws), args.steps, args.warmup)
         mita.mita_device_status(ws)
-        ms = e0.elapsed_time(e1) / args.steps
         F, Bytes = work_counts(w)
         t_f, t_b = F / (pk["bf16_tflops"] * 1e12), Bytes / (pk["hbm_gbs"] * 1e9)
         t_roof = max(t_f, t_b)
@@ -458,16 +460,46 @@ def pinned_host(nbytes, torch):
         return torch.empty(nbytes, dtype=torch.uint8).pin_memory(), "torch pin_memory"
 
 
+def capture_forward(mita, torch, p, Q, K, V, O, ws):
+    """One mita_forward on the current stream captured as a CUDA graph, and the
+    number of this library's kernels in it (counted by the library during the
+    capture; every replay launches the same kernels)."""
+    n0 = mita.mita_launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+        mita.mita_forward(p, Q, K, V, O, ws)
+    return graph, mita.mita_launch_count() - n0
+
+
+def profile_phases(mita, fn, steps):
+    """Per-phase milliseconds of fn() (the library's phase events), profiled
+    step by step; the median of each phase over `steps` steps."""
+    per = {}
+    for _ in range(steps):
+        mita.mita_profile_begin(64)
+        fn()
+        for k, v in mita.mita_profile_end().items():
+            per.setdefault(k, []).append(v)
+    return {k: statistics.median(v) for k, v in per.items()}
+
+
 def _time_cuda(fn, steps, warmup):
-    """Mean milliseconds of fn() over `steps` calls after `warmup`, CUDA events."""
+    """Mean milliseconds of fn() over `steps` calls after `warmup`, CUDA events;
+    fn is captured once as a CUDA graph and the graph replayed, so that the
+    whole timed region is queued at once (no host stall inside it)."""
     import torch
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+        fn()
+    graph.replay()
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(steps):
-        fn()
+        graph.replay()
     e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / steps
@@ -564,9 +596,9 @@ def backward_arm(args):
     ws = torch.empty(mita.mita_backward_workspace_size(p), dtype=torch.uint8, device=dev)
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     steps = max(3, min(args.steps, 10))
-    mita.mita_profile_begin(16 * (steps + args.warmup) + 16)
-    ms = _time_cuda(lambda: mita.mita_backward(p, Q, K, V, dO, idx, route, dQ, dK, dV, ws), steps, args.warmup)
-    phases = {k_: v_ / (steps + args.warmup) for k_, v_ in mita.mita_profile_end().items()}
+    bwd = lambda: mita.mita_backward(p, Q, K, V, dO, idx, route, dQ, dK, dV, ws)
+    ms = _time_cuda(bwd, steps, args.warmup)
+    phases = profile_phases(mita, bwd, steps)
     mita.mita_device_status(ws)
     slots = w.m + w.s * w.k
     flops = w.BH * w.N * (2.0 * 2 * slots * w.d + 2.0 * 3 * slots * w.d) + w.BH * 8.0 * 2 * w.m * w.N * w.d
