@@ -193,30 +193,6 @@ __device__ __forceinline__ int first_eq64(const float (&v)[64], float x) {
     return c[0];
 }
 
-// The s (<= SMAX) largest of 64 scores v (masked ones at -inf), descending,
-// ties to the lower index, as order keys and indices base + j; m is max64(v).
-// Round u takes the largest remaining score and the lowest index holding it,
-// then masks that entry; v is consumed. Unused slots: key 0, index -1.
-template <int SMAX>
-__device__ __forceinline__ void top_s64(float (&v)[64], float m, int s, int base, uint32_t (&bu)[SMAX],
-                                        int (&bi)[SMAX]) {
-#pragma unroll
-    for (int u = 0; u < SMAX; ++u) {
-        bu[u] = 0u;
-        bi[u] = -1;
-        if (u < s && m > -INFINITY) {
-            const int i = first_eq64(v, m);
-            bu[u] = order_key(m);
-            bi[u] = base + i;
-            if (u + 1 < s) {
-#pragma unroll
-                for (int j = 0; j < 64; ++j) v[j] = j == i ? -INFINITY : v[j];
-                m = max64(v);
-            }
-        }
-    }
-}
-
 }  // namespace
 
 // Sample pass of the top-k selection: raw scores of each landmark row against
@@ -757,37 +733,33 @@ __global__ void __launch_bounds__(256, 1)
     if (threadIdx.x < 32) tmem_dealloc(tmem, tmem_cols);
 }
 
-// Routing + shared slots, warp-specialized and persistent (m_pad == 128):
-//   warps 0-7  two warpgroups, one per half of the 128 landmark columns: each
-//              keeps the s best landmarks of its half and the halves merge in
-//              a fixed order (ties to the lower landmark index); the softmax
-//              over the shared logits shares its row max / sum the same way
-//   warp 8     producer: TMA loads of consecutive 128-query tiles (NSQ-stage
-//              ring); the head's Qt (hi, lo) and Vt when the head changes
-//   warp 9     MMA issuer: R = Q Qhi^T + Q Qlo^T into one of two TMEM
-//              buffers; P Vt (P over R in TMEM) into one of two outputs
+// Routing + shared slots with two query tiles in flight (m_pad == 128): each
+// softmax warpgroup owns every other tile of the CTA and holds whole rows (one
+// query per thread), so its routing choice and its softmax over the shared
+// logits need no exchange with the other warpgroup, and the two run out of
+// phase: one's exponentials overlap the other's routing, epilogue stores and
+// MMAs. Warpgroup w: TMEM columns 128 w (R, then P over it) and 256 + 128 w
+// (the shared-slot output). The producer warp loads consecutive 128-query
+// tiles by TMA (NSQ-stage ring) and the head's Qt (hi, lo) and Vt by cp.async
+// when the head changes; the old landmarks are released once every older tile
+// (the other warpgroup's last one) has its P Vt issued.
 template <int D, int SMAX, int NSQ>
 __global__ void __launch_bounds__(320, 1)
-    k_route_ws(const __grid_constant__ CUtensorMap tmQ, const __nv_bfloat16* __restrict__ Qhi,
+    k_route_pp(const __grid_constant__ CUtensorMap tmQ, const __nv_bfloat16* __restrict__ Qhi,
                const __nv_bfloat16* __restrict__ Qlo, const __nv_bfloat16* __restrict__ Vtb, int N, int m, int s,
                int tiles_per_head, int total_tiles, float sl, int causal, int32_t* __restrict__ E,
                __nv_bfloat16* __restrict__ sh_part, float* __restrict__ sh_lse, int* __restrict__ status) {
     constexpr int TILE = kT * D * 2;
-    constexpr int DH = D / 2;
-    constexpr uint32_t kR0 = 0, kO0 = 256;  // TMEM: R/P buffers 0 / 128, outputs 256 / 256 + D
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sHi = sm;
     uint8_t* sLo = sm + TILE;
     uint8_t* sVt = sm + 2 * TILE;
-    uint8_t* sQ = sm + 3 * TILE;  // NSQ stages
+    uint8_t* sQ = sm + 3 * TILE;        // NSQ stages
     uint8_t* sStage = sQ + NSQ * TILE;  // 8 x kStageWarp epilogue staging
     __shared__ uint64_t q_full[NSQ], q_empty[NSQ], r_full[2], p_full[2], o_full[2], o_free[2];
-    __shared__ uint64_t lm_full, lm_free, xbar, ebar, kbar;  // lm_free: the MMA warp is done with a head's landmarks
+    __shared__ uint64_t lm_full, lm_free, drain;
     __shared__ int qgen[NSQ];  // landmark load each query tile uses (1-based)
-    __shared__ float xmax[2][2][kT], xl[2][2][kT];  // [tile parity][half][row]
-    __shared__ uint32_t xkey[kT][SMAX];  // the second half's s best, handed to the first
-    __shared__ int xidx[kT][SMAX];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     volatile int* abort_v = &abort_flag;
@@ -804,15 +776,13 @@ __global__ void __launch_bounds__(320, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&r_full[i], 1);
-            mbar_init(&p_full[i], 8);
+            mbar_init(&p_full[i], 4);
             mbar_init(&o_full[i], 1);
-            mbar_init(&o_free[i], 8);
+            mbar_init(&o_free[i], 4);
         }
         mbar_init(&lm_full, 32);
         mbar_init(&lm_free, 1);
-        mbar_init(&xbar, 8);
-        mbar_init(&ebar, 8);
-        mbar_init(&kbar, 4);
+        mbar_init(&drain, 1);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -829,8 +799,6 @@ __global__ void __launch_bounds__(320, 1)
         for (int tl = 0; tl < nloc; ++tl) {
             const int bh = head(tl);
             const bool reload = bh != cur;
-            // the query tile first: the MMA warp needs it to issue the previous
-            // tile's deferred P Vt, which the landmark reload below waits for
             const int st = tl % NSQ;
             int okw = 1;
             if (lane == 0) okw = ws_wait(&q_empty[st], ((tl / NSQ) & 1) ^ 1, status, abort_v);
@@ -868,186 +836,217 @@ __global__ void __launch_bounds__(320, 1)
         cp_async_wait_all();
     } else if (warp == 9) {
         // ------------------------------------------------------ MMA issuer
+        // One thread polls without blocking. Per warpgroup w (tiles tl = 2 j + w):
+        // R of tile j once its R buffer is free (P Vt of tile j - 1 issued), its
+        // query tile is in and its landmarks are loaded; P Vt of tile j once its
+        // probabilities are in and the epilogue of tile j - 1 has read O.
         if (lane == 0) {
-            bool ok = true, pending = false;
-            int ptl = 0, cur_gen = 0;
-            auto flush = [&]() -> bool {
-                const int ob = ptl & 1;
-                if (!ws_wait(&p_full[ptl & 1], (ptl >> 1) & 1, status, abort_v)) return false;
-                if (!ws_wait(&o_free[ob], ((ptl >> 1) & 1) ^ 1, status, abort_v)) return false;
-                fence_after_sync();
-                issue_pv_ts<D>(tmem + kO0 + ob * D, tmem + kR0 + (ptl & 1) * 128, smem_u32(sVt), false);
-                mma_commit(&o_full[ob]);
-                pending = false;
-                return true;
-            };
-            for (int tl = 0; tl < nloc; ++tl) {
-                const int st = tl % NSQ, rb = tl & 1;
-                if (!(ok = ws_wait(&q_full[st], (tl / NSQ) & 1, status, abort_v))) break;
-                const int gen = qgen[st];
-                if (gen != cur_gen) {
-                    // new landmarks: the previous tile's P Vt first, then release the old
-                    // landmarks (the commit arrives when every MMA so far is done)
-                    if (pending && !(ok = flush())) break;
-                    if (cur_gen > 0) mma_commit(&lm_free);
-                    if (!(ok = ws_wait(&lm_full, (gen - 1) & 1, status, abort_v))) break;
-                    fence_proxy_async();  // landmarks came through cp.async (generic proxy)
-                    cur_gen = gen;
+            int nR[2] = {0, 0}, nP[2] = {0, 0};
+            const int G[2] = {(nloc + 1) / 2, nloc / 2};
+            int cur_gen = 0, rel = 0;
+            long long idle0 = clock64();
+            while (nP[0] < G[0] || nP[1] < G[1]) {
+                bool prog = false;
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    if (nR[w] < G[w] && nR[w] == nP[w]) {
+                        const int j = nR[w], tl = 2 * j + w, st = tl % NSQ;
+                        if (mbar_test_wait(&q_full[st], (tl / NSQ) & 1)) {
+                            const int gen = qgen[st];
+                            bool ready = true;
+                            if (gen == cur_gen + 1) {
+                                if (cur_gen > 0 && rel < cur_gen) {
+                                    // release the old landmarks once the other warpgroup's last
+                                    // older tile has its P Vt issued, or waits for the new
+                                    // landmarks itself (then its older tiles are all done)
+                                    const int wo = w ^ 1, jo = (tl - 1) >> 1;
+                                    const bool done_o = nP[wo] > jo ||
+                                                        (nR[wo] == jo && nP[wo] == jo && qgen[(tl - 1) % NSQ] == gen);
+                                    if (done_o) {
+                                        mma_commit(&lm_free);
+                                        ++rel;
+                                        prog = true;
+                                    } else {
+                                        ready = false;
+                                    }
+                                }
+                                if (ready) {
+                                    if (mbar_test_wait(&lm_full, (gen - 1) & 1)) {
+                                        cur_gen = gen;
+                                        fence_proxy_async();  // landmarks came through cp.async (generic proxy)
+                                        prog = true;
+                                    } else {
+                                        ready = false;
+                                    }
+                                }
+                            } else if (gen != cur_gen) {
+                                ready = false;  // the other warpgroup's older tile moves the landmarks first
+                            }
+                            if (ready) {
+                                fence_after_sync();
+                                issue_qk<D>(tmem + w * 128, smem_u32(sQ + st * TILE), smem_u32(sHi), false);
+                                issue_qk<D>(tmem + w * 128, smem_u32(sQ + st * TILE), smem_u32(sLo), true);
+                                mma_commit(&r_full[w]);
+                                mma_commit(&q_empty[st]);
+                                ++nR[w];
+                                prog = true;
+                            }
+                        }
+                    }
+                    if (nP[w] < nR[w]) {
+                        const int j = nP[w];
+                        if (mbar_test_wait(&p_full[w], j & 1) && mbar_test_wait(&o_free[w], (j & 1) ^ 1)) {
+                            fence_after_sync();
+                            issue_pv_ts<D>(tmem + 256 + w * 128, tmem + w * 128, smem_u32(sVt), false);
+                            mma_commit(&o_full[w]);
+                            ++nP[w];
+                            prog = true;
+                        }
+                    }
                 }
-                fence_after_sync();
-                issue_qk<D>(tmem + kR0 + rb * 128, smem_u32(sQ + st * TILE), smem_u32(sHi), false);
-                issue_qk<D>(tmem + kR0 + rb * 128, smem_u32(sQ + st * TILE), smem_u32(sLo), true);
-                mma_commit(&r_full[rb]);
-                mma_commit(&q_empty[st]);
-                if (pending && !(ok = flush())) break;
-                pending = true;
-                ptl = tl;
+                if (prog) {
+                    idle0 = clock64();
+                } else {
+                    if (*abort_v) break;
+                    if (clock64() - idle0 > kSpin) {
+                        set_status(status, kStTimeout);
+                        *abort_v = 1;
+                        break;
+                    }
+                }
             }
-            if (ok && pending) flush();
+            // every MMA this thread issued has completed before TMEM is freed
+            mma_commit(&drain);
+            drain_wait(&drain, 0, status);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------- softmax + epilogue
-        // a tile's epilogue (its normalized shared-slot partial) runs after the
-        // next tile's scores, so its P Vt has had that long to finish
-        const int wg = warp >> 2, r = threadIdx.x & 127;
+        const int w = warp >> 2, r = threadIdx.x & 127;
         uint8_t* stage = sStage + warp * kStageWarp;
-        // lt: the whole row sum when the halves already exchanged it (with the next
-        // tile's row maxima); last: the CTA's last tile, whose epilogue
-        // exchanges the row sum itself
-        auto epilogue = [&](int pt, float lsum, float mx, float lt, bool last) -> bool {
-            constexpr int PPR = DH / 8, RPI = 32 / PPR;  // pieces per half row, rows per store instruction
-            const int ob = pt & 1;
-            const int bh = head(pt), q0 = ((t_begin + pt) % tiles_per_head) * kT, q = q0 + r;
-            if (!__all_sync(0xffffffffu, ws_wait(&o_full[ob], (pt >> 1) & 1, status, abort_v))) return false;
-            fence_after_sync();
-            float o[DH];
-#pragma unroll
-            for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(lane_base(tmem) + kO0 + ob * D + wg * DH + c0, o + c0);
-            tmem_wait_ld();
-            if (last) xl[pt & 1][wg][r] = lsum;
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&o_free[ob]);
-                if (last) mbar_arrive(&ebar);
-            }
-            if (last) {  // ebar's only use
-                if (!__all_sync(0xffffffffu, ws_wait(&ebar, 0, status, abort_v))) return false;
-                lt = lsum + xl[pt & 1][wg ^ 1][r];
-            }
-            const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;  // no slot (causal only): zero partial
-            const size_t row0 = (size_t)bh * N + q0 + (r & ~31);  // this warp's first row
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {  // lanes 16h .. 16h + 15 stage their rows
-                if ((lane >> 4) == h) {
-#pragma unroll
-                    for (int u = 0; u < PPR; ++u) {
-                        const float* x = o + 8 * u;
-                        *reinterpret_cast<uint4*>(stage + stage_off<PPR>(lane & 15, u)) =
-                            make_uint4(pack_bf16(x[0] * inv, x[1] * inv), pack_bf16(x[2] * inv, x[3] * inv),
-                                       pack_bf16(x[4] * inv, x[5] * inv), pack_bf16(x[6] * inv, x[7] * inv));
-                    }
-                }
-                __syncwarp();
-#pragma unroll
-                for (int i = 0; i < 16 / RPI; ++i) {
-                    const int rl = 16 * h + i * RPI + lane / PPR, u = lane % PPR;
-                    const uint4 w4 = *reinterpret_cast<const uint4*>(stage + stage_off<PPR>(rl - 16 * h, u));
-                    if (q0 + (r & ~31) + rl < N)
-                        *reinterpret_cast<uint4*>(sh_part + (row0 + rl) * D + wg * DH + 8 * u) = w4;
-                }
-                __syncwarp();
-            }
-            if (wg == 0 && q < N) sh_lse[(size_t)bh * N + q] = lt > 0.0f ? mx + __log2f(lt) : -INFINITY;
-            return true;
-        };
-        bool ok = true;
-        float plsum = 0.0f, pmx = 0.0f;
-        for (int tl = 0; tl < nloc; ++tl) {
-            const int rb = tl & 1;
-            const int bh = head(tl), q = ((t_begin + tl) % tiles_per_head) * kT + r;
+        const uint32_t tR = lane_base(tmem) + w * 128, tO = lane_base(tmem) + 256 + w * 128;
+        for (int j = 0;; ++j) {
+            const int tl = 2 * j + w;
+            if (tl >= nloc) break;
+            const int bh = head(tl), q0 = ((t_begin + tl) % tiles_per_head) * kT, q = q0 + r;
             const bool q_ok = q < N;
-            if (!__all_sync(0xffffffffu, ws_wait(&r_full[rb], (tl >> 1) & 1, status, abort_v))) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, ws_wait(&r_full[w], j & 1, status, abort_v))) break;
             fence_after_sync();
-            const uint32_t tR = lane_base(tmem) + kR0 + rb * 128;
-            const int nval = min(64, m - 64 * wg);  // landmarks of this half
             // causal variant: the shared slots are the landmarks whose bin is
             // complete at query q (a prefix of the landmarks); routing still
             // ranks all of them
-            const int nsm = causal ? min(nval, landmarks_complete(q_ok ? q : N - 1, N, m) - 64 * wg) : nval;
-            float v[64];
-            tmem_ld32(tR + 64 * wg, v);
-            tmem_ld32(tR + 64 * wg + 32, v + 32);
-            tmem_wait_ld();
-            // this half's landmarks only: the others at -inf
+            const int nsm = causal ? min(m, landmarks_complete(q_ok ? q : N - 1, N, m)) : m;
+            // pass 1, 64 columns at a time: the s best landmarks (ties to the lower
+            // index) and the largest shared-slot logit
+            uint32_t bu[SMAX];
+            int bi[SMAX];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) v[j] = j < nval ? v[j] : -INFINITY;
-            const float hmax = max64(v);  // largest raw score of this half
-            float mx = hmax * sl;
-            if (!(sl > 0.0f) || nsm < nval) {  // a negative scale turns the smallest score into the largest
-                mx = -INFINITY;               // logit; a causal row has fewer slots
-#pragma unroll
-                for (int j = 0; j < 64; ++j) mx = fmaxf(mx, j < nsm ? v[j] * sl : -INFINITY);
+            for (int u = 0; u < SMAX; ++u) {
+                bu[u] = 0u;
+                bi[u] = -1;
             }
-            xmax[tl & 1][wg][r] = mx;
-            if (tl > 0) xl[(tl - 1) & 1][wg][r] = plsum;  // the previous tile's row-sum half
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&xbar);
-            if (!__all_sync(0xffffffffu, ws_wait(&xbar, tl & 1, status, abort_v))) { ok = false; break; }
-            fence_after_sync();
-            mx = fmaxf(mx, xmax[tl & 1][wg ^ 1][r]);
-            float lsum = 0.0f;
-            uint32_t pkd[32];
-            if (nval > 0) {
+            float mx = -INFINITY;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kT; c0 += 64) {
+                float v[64];
+                tmem_ld32(tR + c0, v);
+                tmem_ld32(tR + c0 + 32, v + 32);
+                tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 64; j += 2) {
-                    const float e0 = ex2(fmaf(v[j], sl, -mx)), e1 = ex2(fmaf(v[j + 1], sl, -mx));
-                    const float p0 = j < nsm ? e0 : 0.0f, p1 = j + 1 < nsm ? e1 : 0.0f;
-                    lsum += p0 + p1;
-                    pkd[j >> 1] = pack_bf16(p0, p1);
+                for (int jj = 0; jj < 64; ++jj) v[jj] = c0 + jj < m ? v[jj] : -INFINITY;
+                float bmx = max64(v);
+                if (sl > 0.0f && nsm >= min(m, c0 + 64)) {
+                    mx = fmaxf(mx, bmx * sl);
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 64; ++jj) mx = fmaxf(mx, c0 + jj < nsm ? v[jj] * sl : -INFINITY);
                 }
-            } else {  // this half holds no landmark (m <= 64)
+#pragma unroll 1
+                for (int u = 0; u < SMAX; ++u) {
+                    if (!(bmx > -INFINITY) || order_key(bmx) <= bu[SMAX - 1]) break;
+                    const int i = first_eq64(v, bmx);
+                    top_insert<SMAX>(bu, bi, order_key(bmx), c0 + i);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) pkd[j] = 0u;
+                    for (int jj = 0; jj < 64; ++jj) v[jj] = jj == i ? -INFINITY : v[jj];
+                    bmx = max64(v);
+                }
             }
-            tmem_st32(tR + 32 * wg, reinterpret_cast<const float*>(pkd));
+            // pass 2: the probabilities, P of keys 0..63 over columns 0..31 (scores
+            // read), then of keys 64..127 over columns 32..63
+            float l = 0.0f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kT; c0 += 64) {
+                float v[64];
+                tmem_ld32(tR + c0, v);
+                tmem_ld32(tR + c0 + 32, v + 32);
+                tmem_wait_ld();
+                float s0 = 0.0f, s1 = 0.0f;
+                uint32_t pkd[32];
+#pragma unroll
+                for (int jj = 0; jj < 64; jj += 2) {
+                    const float e0 = ex2(fmaf(v[jj], sl, -mx)), e1 = ex2(fmaf(v[jj + 1], sl, -mx));
+                    const float p0 = c0 + jj < nsm ? e0 : 0.0f, p1 = c0 + jj + 1 < nsm ? e1 : 0.0f;
+                    if (jj & 2) s1 += p0 + p1;
+                    else s0 += p0 + p1;
+                    pkd[jj >> 1] = pack_bf16(p0, p1);
+                }
+                l += s0 + s1;
+                tmem_st32(tR + (c0 >> 1), reinterpret_cast<const float*>(pkd));
+            }
             tmem_wait_st();
             fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[rb]);
-            // routes: this half's s best (v is consumed), the second half's list
-            // handed to the first, which merges it after its own (higher indices)
-            uint32_t bu[SMAX];
-            int bi[SMAX];
-            top_s64<SMAX>(v, hmax, s, 64 * wg, bu, bi);
-            if (wg == 1) {
+            if (lane == 0) mbar_arrive(&p_full[w]);
+            if (q_ok) {
+                int32_t* Erow = E + ((size_t)bh * N + q) * s;
 #pragma unroll
-                for (int u = 0; u < SMAX; ++u) {
-                    xkey[r][u] = bu[u];
-                    xidx[r][u] = bi[u];
+                for (int u = 0; u < SMAX; ++u)
+                    if (u < s) Erow[u] = bi[u];
+            }
+            // epilogue: the normalized shared-slot partial row and its log2-sum-exp
+            if (!__all_sync(0xffffffffu, ws_wait(&o_full[w], j & 1, status, abort_v))) break;
+            fence_after_sync();
+            const float inv = l > 0.0f ? 1.0f / l : 0.0f;  // no slot (causal only): zero partial
+            const size_t row0 = (size_t)bh * N + q0 + (r & ~31);  // this warp's first row
+            constexpr int PPR = 8, RPS = 32 / PPR;  // 16-byte pieces per 64-column half row, rows per store
+            // O in halves of 64 columns (registers); the next P Vt of this warpgroup
+            // waits for o_free, but it also needs this warpgroup's next P, which
+            // comes after this epilogue anyway
+#pragma unroll 1
+            for (int hh = 0; hh < D / 64; ++hh) {
+                float o[64];
+                tmem_ld32(tO + 64 * hh, o);
+                tmem_ld32(tO + 64 * hh + 32, o + 32);
+                tmem_wait_ld();
+                if (hh == D / 64 - 1) {
+                    fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&o_free[w]);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&kbar);
-            } else {
-                if (!__all_sync(0xffffffffu, ws_wait(&kbar, tl & 1, status, abort_v))) { ok = false; break; }
-                if (q_ok) {
 #pragma unroll
-                    for (int u = 0; u < SMAX; ++u)
-                        if (xidx[r][u] >= 0) top_insert<SMAX>(bu, bi, xkey[r][u], xidx[r][u]);
-                    int32_t* Erow = E + ((size_t)bh * N + q) * s;
+                for (int h = 0; h < 2; ++h) {  // lanes 16h .. 16h + 15 stage their rows
+                    if ((lane >> 4) == h) {
 #pragma unroll
-                    for (int u = 0; u < SMAX; ++u)
-                        if (u < s) Erow[u] = bi[u];
+                        for (int u = 0; u < PPR; ++u) {
+                            const float* x = o + 8 * u;
+                            *reinterpret_cast<uint4*>(stage + stage_off<PPR>(lane & 15, u)) =
+                                make_uint4(pack_bf16(x[0] * inv, x[1] * inv), pack_bf16(x[2] * inv, x[3] * inv),
+                                           pack_bf16(x[4] * inv, x[5] * inv), pack_bf16(x[6] * inv, x[7] * inv));
+                        }
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 16 / RPS; ++i) {
+                        const int rl = 16 * h + i * RPS + lane / PPR, u = lane % PPR;
+                        const uint4 w4 = *reinterpret_cast<const uint4*>(stage + stage_off<PPR>(rl - 16 * h, u));
+                        if (q0 + (r & ~31) + rl < N)
+                            *reinterpret_cast<uint4*>(sh_part + (row0 + rl) * D + 64 * hh + 8 * u) = w4;
+                    }
+                    __syncwarp();
                 }
             }
-            // the other half posted its share before this tile's exchange
-            if (tl > 0 && !(ok = epilogue(tl - 1, plsum, pmx, plsum + xl[(tl - 1) & 1][wg ^ 1][r], false))) break;
-            plsum = lsum;
-            pmx = mx;
+            if (q_ok) sh_lse[(size_t)bh * N + q] = l > 0.0f ? mx + __log2f(l) : -INFINITY;
         }
-        if (ok && nloc > 0) epilogue(nloc - 1, plsum, pmx, 0.0f, true);
     }
     fence_before_sync();
     __syncthreads();
@@ -2041,11 +2040,11 @@ static cudaError_t launch_route_s(const Dims& D, const TcPlan& P, const TcWork& 
         if ((e = tile_map(&mq, q, (long long)D.BH * D.N, DD))) return e;
         constexpr int NSQ = 3;
         const int smem = (3 + NSQ) * tile + 8 * kStageWarp + 1024;
-        if ((e = set_smem(k_route_ws<DD, SMAX, NSQ>, smem))) return e;
+        if ((e = set_smem(k_route_pp<DD, SMAX, NSQ>, smem))) return e;
         const int tph = (D.N + kT - 1) / kT;
         const int total = tph * D.BH;
         const int grid = std::min(total, num_sms());
-        k_route_ws<DD, SMAX, NSQ><<<grid, 320, smem, st>>>(mq, W.Qhi, W.Qlo, W.Vtb, D.N, D.m, D.s, tph, total,
+        k_route_pp<DD, SMAX, NSQ><<<grid, 320, smem, st>>>(mq, W.Qhi, W.Qlo, W.Vtb, D.N, D.m, D.s, tph, total,
                                                            D.scale * 1.4426950408889634f, D.causal ? 1 : 0, E,
                                                            W.sh_part, W.sh_lse, status);
     } else if (P.m_pad <= 256) {
