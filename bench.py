@@ -35,7 +35,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # a smaller head count scaled to 32 heads. It is tied to the kernel source it
 # was taken on (sha256 of csrc/tc.cu, first 16 hex digits); once that source
 # changes, the figure no longer describes the kernel and the line reports null.
-EXPERT_TRAFFIC = {"kernel": "k_expert_res", "tc_cu_sha16": "c7750e2661d24fbb", "bytes_per_launch": 129.8e6 * 32 / 6,
+EXPERT_TRAFFIC = {"kernel": "k_expert_res", "src_sha16": "0000000000000000", "bytes_per_launch": 129.8e6 * 32 / 6,
                   "how": "ncu dram__bytes.sum of one launch on the 6-head case (129.8 MB), scaled by 32 / 6 heads"}
 
 
@@ -63,10 +63,15 @@ def expert_flops(w):
     return 4.0 * w.BH * w.N * w.d * w.s * w.k
 
 
-def tc_cu_sha16():
+def expert_src_sha16():
+    """Hash of the expert kernel's source (tc.cu from its tile descriptor to
+    the host code): the stored traffic figure belongs to that source only."""
     import hashlib
-    with open(os.path.join(ROOT, "compressed_attention_adaptive_gb300", "csrc", "tc.cu"), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(os.path.join(ROOT, "compressed_attention_adaptive_gb300", "csrc", "tc.cu")) as f:
+        src = f.read()
+    a = src.index("struct ResTile {")
+    b = src.index("// ------------------------------------------------------------------ host", a)
+    return hashlib.sha256(src[a:b].encode()).hexdigest()[:16]
 
 
 def cpu_model():
@@ -264,7 +269,7 @@ def expert_roofline(w, phase_ms, pk, pk_src, ms_step):
     achieved = flops / (ms * 1e-3) / 1e12
     kernel = "k_expert_res"
     traffic = None
-    if EXPERT_TRAFFIC["kernel"] == kernel and EXPERT_TRAFFIC["tc_cu_sha16"] == tc_cu_sha16() \
+    if EXPERT_TRAFFIC["kernel"] == kernel and EXPERT_TRAFFIC["src_sha16"] == expert_src_sha16() \
             and w.name == "longctx_n32k":
         traffic = EXPERT_TRAFFIC["bytes_per_launch"]
     peak = pk["bf16_tflops"]
