@@ -36,6 +36,10 @@ SMALL = [
     L["fp32_n1024"].with_(N=777, m=5, k=123, s=2, d=32),
     L["longctx_n32k"].with_(B=1, H=1, N=640, m=1, k=1, s=1),
     L["longctx_n32k"].with_(B=1, H=1, N=256, m=256, k=256, s=8),
+    # experts cut into ragged 256-key sub-experts, and more than 256 landmarks
+    # (the shared slots' own pass, also in ragged parts)
+    L["n131k"].with_(B=1, H=1, N=4096, m=300, k=600, s=3),
+    L["longctx_n32k"].with_(B=1, H=2, N=3000, d=64, m=200, k=520, s=2),
 ]
 
 
