@@ -303,6 +303,8 @@ def main():
                          "forward over N = 4k .. 128k at the long-context head shape, one JSON line per N")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (CUDA cores, fp32) on the long-context head shape at B=1, H=2")
+    ap.add_argument("--causal", action="store_true",
+                    help="time the causal variant on the long-context workload against its own roofline")
     ap.add_argument("--inference-mk", action="store_true",
                     help="time the MiTA forward on one fixed input while m and k grow beyond the training values "
                          "(the pages' inference-time knob), one JSON line per (m, k)")
@@ -319,6 +321,9 @@ def main():
         return
     if args.backward:
         backward_arm(args)
+        return
+    if args.causal:
+        causal_arm(args)
         return
 
     from compressed_attention_adaptive_gb300 import synth
@@ -579,6 +584,59 @@ def inference_mk(args):
                           "rel_change_vs_m128_k256": float((Of - ref).norm() / ref.norm())}), flush=True)
         del O, ws
         torch.cuda.empty_cache()
+
+
+def causal_arm(args):
+    """The causal variant on the long-context workload (B=2, H=16, N=32768,
+    m=128, k=256, s=2): time per forward and its roofline with the causal
+    variant's own algorithmic flops: the shared expert of landmark i over the
+    keys before its bin's end, the first floor((t + 1) m / N) shared slots of
+    query t, and of each routed expert the keys at or before t (counted on the
+    sets and routes this forward chose)."""
+    import numpy as np
+    import torch
+    import compressed_attention_adaptive_gb300 as mita
+    from compressed_attention_adaptive_gb300 import synth
+    dev = torch.device("cuda", 0)
+    pk, pk_src = peaks()
+    w = synth.get("longctx_n32k")
+    Qn, Kn, Vn = synth.make_inputs(w, seed=0)
+    tt = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    Q, K, V = tt(Qn), tt(Kn), tt(Vn)
+    O = torch.empty_like(Q)
+    p = mita.params_for(Q, w.m, w.k, w.s)
+    p.flags |= mita.FLAG_CAUSAL
+    ws = mita.workspace(p, dev)
+    idx = torch.empty((w.BH, w.m, w.k), dtype=torch.int32, device=dev)
+    route = torch.empty((w.BH, w.N, w.s), dtype=torch.int32, device=dev)
+    mita.mita_forward(p, Q, K, V, O, ws, idx_out=idx, route_out=route)
+    torch.cuda.synchronize()
+    mita.mita_device_status(ws)
+    fwd = lambda: mita.mita_forward(p, Q, K, V, O, ws)
+    ms = _time_cuda(fwd, max(3, min(args.steps, 50)), args.warmup)
+    phases = profile_phases(mita, fwd, max(3, min(args.steps, 30)))
+    mita.mita_device_status(ws)
+    # algorithmic flops of the causal variant (4 d per query-key pair: q.k and p.v)
+    N, m, d = w.N, w.m, w.d
+    hi = np.minimum(N, ((np.arange(m) + 1) * N + m - 1) // m)  # landmark bins' ends
+    shared_expert = 4.0 * d * hi.sum()
+    t = np.arange(N)
+    shared_slots = 4.0 * d * ((t + 1) * m // N).sum()
+    routed = 0.0
+    tq = torch.arange(N, device=dev, dtype=torch.int32)
+    for bh in range(w.BH):
+        rows = idx[bh][route[bh].long()]  # [N, s, k] ascending key indices of each routed expert
+        routed += 4.0 * d * float(torch.searchsorted(rows.reshape(N * w.s, w.k).contiguous(),
+                                                     tq.repeat_interleave(w.s).reshape(-1, 1),
+                                                     right=True).sum())
+    F = w.BH * (shared_expert + shared_slots) + routed
+    _, Bytes = work_counts(w)
+    t_roof = max(F / (pk["bf16_tflops"] * 1e12), Bytes / (pk["hbm_gbs"] * 1e9))
+    print(json.dumps({"workload": "longctx_n32k causal", "B": w.B, "H": w.H, "N": N, "d": d, "m": m, "k": w.k,
+                      "s": w.s, "ms": ms, "value": w.BH * N / (ms * 1e-3), "unit": UNIT, "flops": F,
+                      "flops_non_causal": work_counts(w)[0], "t_roof_us": t_roof * 1e6,
+                      "frac": t_roof / (ms * 1e-3), "phases_ms": phases,
+                      "timed_as": "CUDA graph replays of the forward pass"}), flush=True)
 
 
 def backward_arm(args):
