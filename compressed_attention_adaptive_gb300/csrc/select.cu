@@ -142,6 +142,69 @@ __global__ void __launch_bounds__(512) k_sample_threshold(const float* __restric
     }
 }
 
+// Rows of the warp-per-row selects handled by one block (at most).
+constexpr int kRowsPerBlock = 8;
+
+// Warp-level MSD radix select: the largest key v such that at least `rem` of
+// the keys key_of accepts are >= v (four 8-bit digit passes over the keys that
+// each(f) hands the warp's lanes, f(u, j) per key, with the warp's own 256-bin
+// histogram). Returns v; *rem_out = how many keys equal to v are still needed,
+// *eq_out = how many accepted keys equal v.
+template <typename Each, typename KeyOf>
+__device__ __forceinline__ uint32_t warp_radix_select(Each each, KeyOf key_of, int rem, unsigned* hist, int* rem_out,
+                                                      int* eq_out) {
+    const int lane = threadIdx.x & 31;
+    uint32_t prefix = 0u, mask = 0u;
+    int eq = 0;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int b = lane; b < 256; b += 32) hist[b] = 0u;
+        __syncwarp();
+        each([&](uint32_t u0, int j) {
+            bool ok;
+            const uint32_t u = key_of(u0, j, &ok);
+            if (ok && (u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+        });
+        __syncwarp();
+        int b = 0, above = 0, in_b = 0;
+        const bool found = radix_digit(hist, rem, &b, &above, &in_b);
+        const int src = __ffs(__ballot_sync(0xffffffffu, found)) - 1;
+        b = __shfl_sync(0xffffffffu, b, src);
+        above = __shfl_sync(0xffffffffu, above, src);
+        in_b = __shfl_sync(0xffffffffu, in_b, src);
+        prefix |= (uint32_t)b << shift;
+        rem -= above;
+        eq = in_b;
+        mask |= 0xFFu << shift;
+        __syncwarp();  // every lane has read the histogram before the next pass clears it
+    }
+    *rem_out = rem;
+    *eq_out = eq;
+    return prefix;
+}
+
+// The same threshold with one warp per row and no block-wide barrier, for rows
+// of at most 4096 samples (where it measured faster than a block per row); the
+// row is read once per digit pass (16 KB at n_samp = 4096, from L1/L2).
+__global__ void __launch_bounds__(32 * kRowsPerBlock) k_sample_threshold_w(const float* __restrict__ Ssamp,
+                                                                         long long rows, int n_samp, int k,
+                                                                         float* __restrict__ thr) {
+    __shared__ unsigned hist_all[kRowsPerBlock][256];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * kRowsPerBlock + warp;
+    if (row >= rows) return;  // the whole warp: nothing below syncs the block
+    const float* s = Ssamp + row * n_samp;
+    auto each = [&](auto f) {
+        for (int j = lane; j < n_samp; j += 32) f(order_key(s[j]), j);
+    };
+    int rem, eq;
+    const uint32_t v = warp_radix_select(each, [](uint32_t u, int, bool* ok) { *ok = true; return u; }, k,
+                                         hist_all[warp], &rem, &eq);
+    if (lane == 0) {
+        const float t = key_float(v);
+        thr[row] = t - 1e-3f * fmaxf(1.0f, fabsf(t));
+    }
+}
+
 // Candidates of one row as (order key, key index) pairs: either staged in
 // shared memory (n of them) or read from the `splits` record regions in
 // global memory (region sp holding counts[sp] records at base + sp * cap).
@@ -313,6 +376,12 @@ __global__ void __launch_bounds__(512) k_topk_cand(const int2* __restrict__ cand
 
 cudaError_t launch_sample_threshold(const float* Ssamp, long long rows, int n_samp, int k, float* thr,
                                     cudaStream_t st) {
+    if (n_samp <= 4096) {
+        k_sample_threshold_w<<<(unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock), 32 * kRowsPerBlock, 0, st>>>(
+            Ssamp, rows, n_samp, k, thr);
+        count_launch();
+        return cudaGetLastError();
+    }
     const int bytes = n_samp * 4;
     const int staged = bytes <= 96 * 1024;
     if (staged) {
