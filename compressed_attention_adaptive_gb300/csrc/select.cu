@@ -279,7 +279,8 @@ constexpr int kMaxRegions = 256;
 // memory: ceil(N / 32) bitmap words, then room for `stage_cap` staged
 // candidates (key and index arrays); rows with more candidates are read from
 // global memory on every pass instead.
-__global__ void __launch_bounds__(512) k_topk_cand(const int2* __restrict__ cand, const int* __restrict__ ccount,
+template <int TB>
+__global__ void __launch_bounds__(TB) k_topk_cand(const int2* __restrict__ cand, const int* __restrict__ ccount,
                                                    int splits, long long cap, int m, int m_pad, int N, int k,
                                                    int stage_cap, int32_t* __restrict__ I, int* __restrict__ status) {
     extern __shared__ uint32_t dyn[];
@@ -401,9 +402,16 @@ cudaError_t launch_topk_cand(const int2* cand, const int* ccount, int splits, lo
     const long long want = std::min<long long>(12288, std::max<long long>(1024, 3 * expect));
     const int stage_cap = (int)std::max<long long>(0, std::min<long long>(want, (160 * 1024 - bitmap) / 8));
     const int smem = bitmap + stage_cap * 8;
-    cudaError_t e0 = cudaFuncSetAttribute(k_topk_cand, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // rows of 2^17 keys or more (4096 bitmap words, several times more candidates
+    // per row) run faster with 1024 threads, smaller ones with 512 (measured)
+    auto run = [&](auto kern, int tb) -> cudaError_t {
+        cudaError_t e0 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e0 != cudaSuccess) return e0;
+        kern<<<dim3(m, BH), tb, smem, st>>>(cand, ccount, splits, cap, m, m_pad, N, k, stage_cap, I, status);
+        return cudaSuccess;
+    };
+    cudaError_t e0 = N >= (1 << 17) ? run(k_topk_cand<1024>, 1024) : run(k_topk_cand<512>, 512);
     if (e0 != cudaSuccess) return e0;
-    k_topk_cand<<<dim3(m, BH), 512, smem, st>>>(cand, ccount, splits, cap, m, m_pad, N, k, stage_cap, I, status);
     count_launch();
     return cudaGetLastError();
 }
