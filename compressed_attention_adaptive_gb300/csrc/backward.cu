@@ -82,7 +82,7 @@ cudaError_t gemm(const TA* A, long long sA, long long a_i, long long a_k, const 
                  cudaStream_t st) {
     const long long tiles = (long long)((Nn + 63) / 64) * ((M + 63) / 64) * batch;
     int ksplit = 1;
-    while (tiles * ksplit < 2 * 148 && (K + 2 * ksplit - 1) / (2 * ksplit) >= 256) ksplit *= 2;
+    while (tiles * ksplit < 2 * 152 && (K + 2 * ksplit - 1) / (2 * ksplit) >= 256) ksplit *= 2;
     cudaError_t e;
     if (ksplit > 1 && !accumulate) {  // the split results add up into a cleared C
         for (int b = 0; b < batch; ++b)

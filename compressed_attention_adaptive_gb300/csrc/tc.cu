@@ -1943,7 +1943,7 @@ static int num_sms() {
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 148;
+        if (n <= 0) n = 152;
     }
     return n;
 }
@@ -1953,7 +1953,7 @@ TcPlan tc_plan(const Dims& D) {
     p.m_pad = (D.m + kT - 1) / kT * kT;
     p.m_tiles = p.m_pad / kT;
     const int nchunks = (D.N + kT - 1) / kT;
-    const long long target = 4LL * 148;
+    const long long target = 4LL * 152;  // four CTAs per SM of a GB300
     long long sp = (target + (long long)D.BH * p.m_tiles - 1) / ((long long)D.BH * p.m_tiles);
     if (sp < 1) sp = 1;
     if (sp > 128) sp = 128;  // <= 256 candidate regions per row (two column halves per split) stay stageable
