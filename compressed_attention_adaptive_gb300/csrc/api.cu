@@ -341,7 +341,7 @@ size_t mita_host_buffer_size(const mita_params* p) {
 constexpr int kHostGroups = 8;
 struct HostPipe {
     cudaStream_t in = nullptr, out = nullptr;
-    cudaEvent_t ev[2 * kHostGroups + 2] = {};
+    cudaEvent_t ev[2 * (kHostGroups + 1) + 2] = {};
 };
 static std::mutex g_host_mu;
 static HostPipe g_host_pipe[64];
@@ -382,9 +382,23 @@ mita_status mita_forward_host(const mita_params* p, const void* Q, const void* K
     // group g + 1's inputs go in and group g - 1's output comes out (two copy
     // streams) while group g computes on `stream`; the copy streams wait for
     // earlier work on `stream` and join it at the end, so the call stays
-    // ordered on it.
-    const int G = head % 256 ? 1 : std::min(D.BH, kHostGroups);
-    const int hb = (D.BH + G - 1) / G;
+    // ordered on it. Groups of ceil(BH / 8) heads, the last one in two halves:
+    // what runs after the last copy in (the last group's forward pass and copy
+    // out) is then short, while no group is so small that the fixed latency of
+    // its forward pass outlasts its copy in.
+    int gsz[kHostGroups + 1];
+    int G = 0;
+    if (head % 256) {
+        gsz[G++] = D.BH;  // offsets of later heads would break the copies' alignment
+    } else {
+        const int hb = (D.BH + kHostGroups - 1) / kHostGroups;
+        for (int h = 0; h < D.BH; h += hb) gsz[G++] = std::min(hb, D.BH - h);
+        if (gsz[G - 1] >= 2) {
+            const int a = gsz[G - 1];
+            gsz[G - 1] = a - a / 2;
+            gsz[G++] = a / 2;
+        }
+    }
     std::lock_guard<std::mutex> lk(g_host_mu);
     HostPipe* hp = nullptr;
     MITA_CUDA(host_pipe(&hp), "create copy streams");
@@ -392,9 +406,8 @@ mita_status mita_forward_host(const mita_params* p, const void* Q, const void* K
     MITA_CUDA(cudaEventRecord(ev[0], s), "record event");  // earlier work on `stream` first
     MITA_CUDA(cudaStreamWaitEvent(hp->in, ev[0], 0), "order copies");
     MITA_CUDA(cudaStreamWaitEvent(hp->out, ev[0], 0), "order copies");
-    for (int g = 0; g < G; ++g) {
-        const int h0 = g * hb, nh = std::min(hb, D.BH - h0);
-        if (nh <= 0) break;
+    for (int g = 0, h0 = 0; g < G; h0 += gsz[g], ++g) {
+        const int nh = gsz[g];
         const size_t off = (size_t)h0 * head, len = (size_t)nh * head;
         cudaEvent_t ein = ev[1 + 2 * g], erun = ev[2 + 2 * g];
         MITA_CUDA(cudaMemcpyAsync(b + off, hq + off, len, cudaMemcpyHostToDevice, hp->in), "copy Q to device");
@@ -412,8 +425,8 @@ mita_status mita_forward_host(const mita_params* p, const void* Q, const void* K
         MITA_CUDA(cudaStreamWaitEvent(hp->out, erun, 0), "order copy after compute");
         MITA_CUDA(cudaMemcpyAsync(ho + off, b + 3 * t + off, len, cudaMemcpyDeviceToHost, hp->out), "copy O to host");
     }
-    MITA_CUDA(cudaEventRecord(ev[2 * kHostGroups + 1], hp->out), "record event");
-    MITA_CUDA(cudaStreamWaitEvent(s, ev[2 * kHostGroups + 1], 0), "join copy stream");
+    MITA_CUDA(cudaEventRecord(ev[2 * (kHostGroups + 1) + 1], hp->out), "record event");
+    MITA_CUDA(cudaStreamWaitEvent(s, ev[2 * (kHostGroups + 1) + 1], 0), "join copy stream");
     return MITA_OK;
 }
 

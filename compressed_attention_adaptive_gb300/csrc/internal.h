@@ -95,6 +95,8 @@ struct TcWork {
 
 bool tc_supported(const Dims& D);
 TcPlan tc_plan(const Dims& D);
+// SMs of the current device, queried once (152, a GB300's, if the query fails)
+int num_sms();
 cudaError_t launch_forward_tc(const Dims& D, const TcPlan& P, const TcWork& W, const void* Q, const void* K,
                               const void* V, void* O, float* Vt, int32_t* I, int32_t* E, int* status, int upto,
                               cudaStream_t st);

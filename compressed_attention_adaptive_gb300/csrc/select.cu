@@ -377,7 +377,9 @@ __global__ void __launch_bounds__(TB) k_topk_cand(const int2* __restrict__ cand,
 
 cudaError_t launch_sample_threshold(const float* Ssamp, long long rows, int n_samp, int k, float* thr,
                                     cudaStream_t st) {
-    if (n_samp <= 4096) {
+    // a warp per row is faster for many rows of at most 4096 samples, a block
+    // per row for fewer rows (under ~16 per SM: a few heads) or longer ones
+    if (n_samp <= 4096 && rows >= 16LL * num_sms()) {
         k_sample_threshold_w<<<(unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock), 32 * kRowsPerBlock, 0, st>>>(
             Ssamp, rows, n_samp, k, thr);
         count_launch();

@@ -529,27 +529,72 @@ __global__ void __launch_bounds__(320, 1)
 
 // Merges the per-split partials: Vt = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 // Writes Vt fp32 [BH][m][D] and the bf16 copy [BH][m_pad][D] (padding rows 0).
-__global__ void k_vt_combine(const float* __restrict__ Opart, const float2* __restrict__ ML, int splits, int m,
-                             int m_pad, int D, float* __restrict__ Vt, __nv_bfloat16* __restrict__ Vtb) {
+// One block per (landmark row, head): D/4 lanes of four columns times SL split
+// lanes, each split lane summing every SL-th split, then a sum over the split
+// lanes in shared memory (the splits run in parallel, so a head split many
+// ways, as few heads are, costs no longer than one split few ways).
+template <int D>
+__global__ void __launch_bounds__(256) k_vt_combine(const float* __restrict__ Opart, const float2* __restrict__ ML,
+                                                    int splits, int m, int m_pad, float* __restrict__ Vt,
+                                                    __nv_bfloat16* __restrict__ Vtb) {
+    constexpr int CG = D / 4, SL = 256 / CG;
+    __shared__ float4 red[SL][CG];
+    __shared__ float rden[SL], wmax[8];
     const int i = blockIdx.x, bh = blockIdx.y;
-    for (int c = threadIdx.x; c < D; c += blockDim.x) {
-        float out = 0.0f;
-        if (i < m) {
-            float M = -INFINITY;
-            for (int s = 0; s < splits; ++s) M = fmaxf(M, ML[((size_t)bh * splits + s) * m_pad + i].x);
-            float num = 0.0f, den = 0.0f;
-            for (int s = 0; s < splits; ++s) {
-                const size_t o = ((size_t)bh * splits + s) * m_pad + i;
-                const float2 ml = ML[o];
-                if (ml.y == 0.0f) continue;
-                const float w = exp2f(ml.x - M);
-                num += w * Opart[o * D + c];
-                den += w * ml.y;
-            }
-            out = num / den;
-            Vt[((size_t)bh * m + i) * D + c] = out;
+    const int cg = threadIdx.x % CG, sl = threadIdx.x / CG;
+    const size_t o0 = (size_t)bh * splits * m_pad + i;  // ML index of split 0; split s adds s * m_pad
+    float M = -INFINITY;
+    if (i < m)
+        for (int s = threadIdx.x; s < splits; s += 256) M = fmaxf(M, ML[o0 + (size_t)s * m_pad].x);
+#pragma unroll
+    for (int x = 16; x >= 1; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = M;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < 8; ++w) M = fmaxf(M, wmax[w]);
+    float4 num = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float den = 0.0f;
+    if (i < m) {
+        for (int s = sl; s < splits; s += SL) {
+            const size_t o = o0 + (size_t)s * m_pad;
+            const float2 ml = ML[o];
+            if (ml.y == 0.0f) continue;
+            const float w = exp2f(ml.x - M);
+            const float4 v = reinterpret_cast<const float4*>(Opart + o * D)[cg];
+            num.x += w * v.x;
+            num.y += w * v.y;
+            num.z += w * v.z;
+            num.w += w * v.w;
+            den += w * ml.y;
         }
-        Vtb[((size_t)bh * m_pad + i) * D + c] = __float2bfloat16_rn(out);
+    }
+    red[sl][cg] = num;
+    if (cg == 0) rden[sl] = den;
+    __syncthreads();
+    if (sl == 0) {
+        float4 a = red[0][cg];
+        float dd = rden[0];
+#pragma unroll
+        for (int j = 1; j < SL; ++j) {
+            const float4 b = red[j][cg];
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+            dd += rden[j];
+        }
+        float4 out = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (i < m) {
+            out = make_float4(a.x / dd, a.y / dd, a.z / dd, a.w / dd);
+            float* vt = Vt + ((size_t)bh * m + i) * D + 4 * cg;  // a caller's buffer: 4-byte alignment only
+            vt[0] = out.x;
+            vt[1] = out.y;
+            vt[2] = out.z;
+            vt[3] = out.w;
+        }
+        __nv_bfloat162* vb = reinterpret_cast<__nv_bfloat162*>(Vtb + ((size_t)bh * m_pad + i) * D + 4 * cg);
+        vb[0] = __floats2bfloat162_rn(out.x, out.y);
+        vb[1] = __floats2bfloat162_rn(out.z, out.w);
     }
 }
 
@@ -1937,7 +1982,7 @@ __global__ void __launch_bounds__(kResThreads, 1)
 
 // ------------------------------------------------------------------ host
 
-static int num_sms() {
+int num_sms() {
     static int n = 0;
     if (!n) {
         int dev = 0;
@@ -2093,8 +2138,13 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
     {
         const int smem = std::max(3 * tile, 100 * 1024) + 1024;
         if ((e = set_smem(k_sample_tc<DD>, smem))) return e;
-        const int cpc = 4;
-        const int groups = (P.n_samp + cpc * kT - 1) / (cpc * kT);
+        // sample chunks per CTA: the fewest (of one to four) that keep the grid
+        // within one wave of two CTAs per SM, else four; a few heads then
+        // spread over more SMs, and many heads do not spill into a second wave
+        const int nch = (P.n_samp + kT - 1) / kT;
+        int cpc = 1;
+        while (cpc < 4 && (long long)P.m_tiles * ((nch + cpc - 1) / cpc) * D.BH > 2LL * num_sms()) ++cpc;
+        const int groups = (nch + cpc - 1) / cpc;
         k_sample_tc<DD><<<dim3(P.m_tiles, groups, D.BH), 128, smem, st>>>(kk, W.Qhi, W.Qlo, W.Ssamp, D.N, D.m,
                                                                          P.m_pad, P.R, P.n_samp, cpc, status);
         if ((e = cudaGetLastError())) return e;
@@ -2127,7 +2177,7 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
     if (upto >= 2) {
         prof_mark(st, "vt_combine");
         count_launch();
-        k_vt_combine<<<dim3(P.m_pad, D.BH), DD, 0, st>>>(W.Opart, W.ML, P.splits, D.m, P.m_pad, DD, Vt, W.Vtb);
+        k_vt_combine<DD><<<dim3(P.m_pad, D.BH), 256, 0, st>>>(W.Opart, W.ML, P.splits, D.m, P.m_pad, Vt, W.Vtb);
         if ((e = cudaGetLastError())) return e;
     }
     if (!E) return cudaSuccess;
