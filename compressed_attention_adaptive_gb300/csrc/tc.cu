@@ -1437,8 +1437,8 @@ __global__ void __launch_bounds__(kResThreads, 1)
                  const __nv_bfloat16* __restrict__ V, long long kv_head_rows, const int32_t* __restrict__ I,
                  const int32_t* __restrict__ perm, const int4* __restrict__ tiles, const int2* __restrict__ xtl,
                  int nx, int* __restrict__ work_ctr, __nv_bfloat16* __restrict__ part, float* __restrict__ lse, int N,
-                 int m, int k, int s, int ksub, int nsub, int sh_tph, int sh_grp, float sl, int causal, int stall,
-                 int* __restrict__ status) {
+                 int m, int k, int s, int ksub, int nsub, int npc, int sh_tph, int sh_grp, float sl, int causal,
+                 int stall, int* __restrict__ status) {
     constexpr int TILE = kT * D * 2;
     constexpr uint32_t kS0 = 0, kO0 = 256;  // TMEM: S/P buffers 0 / 128, O buffers 256 / 384
     extern __shared__ uint8_t smem_raw[];
@@ -1517,11 +1517,13 @@ __global__ void __launch_bounds__(kResThreads, 1)
                 const int x = atomicAdd(work_ctr, 1);
                 if (x >= nx) return td;
                 if (x == 0 && stall) stall_pending = true;
-                if (I) {  // expert x / nsub, sub-expert x % nsub
-                    const int2 r = xtl[x / nsub];
-                    x_t = r.x;
-                    x_end = r.x + r.y;
-                    x_u = x % nsub;
+                if (I) {  // piece x % npc of sub-expert xu % nsub of expert xu / nsub, xu = x / npc
+                    const int xu = x / npc, pc = x % npc;
+                    const int2 r = xtl[xu / nsub];
+                    const int per = (r.y + npc - 1) / npc;  // tiles per piece (a piece may be empty)
+                    x_t = r.x + pc * per;
+                    x_end = min(r.x + r.y, x_t + per);
+                    x_u = xu % nsub;
                 } else {  // head, sub-expert, group of sh_grp query tiles
                     const int ngrp = (sh_tph + sh_grp - 1) / sh_grp;
                     x_bh = x / (nsub * ngrp);
@@ -2211,14 +2213,19 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
             const int ngrp = (tph + grp - 1) / grp;
             k_expert_res<DD><<<num_sms(), kResThreads, smem, st>>>(
                 q, W.Qhi, W.Vtb, P.m_pad, nullptr, nullptr, nullptr, nullptr, D.BH * P.nsub_sh * ngrp, W.tile_ctr + 2,
-                W.sh_part, W.sh_lse, D.N, D.m, D.m, 1, P.ksub_sh, P.nsub_sh, tph, grp, sl, 0, stall, status);
+                W.sh_part, W.sh_lse, D.N, D.m, D.m, 1, P.ksub_sh, P.nsub_sh, 1, tph, grp, sl, 0, stall, status);
             if ((e = cudaGetLastError())) return e;
             count_launch();
         }
         prof_mark(st, "expert_res");
+        // with few (sub-)experts per SM (a few heads), each is cut into up to
+        // eight pieces of consecutive tiles, so that the largest ones do not
+        // set the kernel's length (a piece reloads its expert's keys)
+        const long long units = (long long)D.BH * D.m * P.nsub, want = 4LL * num_sms();
+        const int npc = (int)std::max(1LL, std::min(8LL, (want + units - 1) / units));
         k_expert_res<DD><<<num_sms(), kResThreads, smem, st>>>(
-            q, kk, v, D.N, I, W.perm, W.tiles, W.xtl, D.BH * D.m * P.nsub, W.tile_ctr + 1, W.part, W.lse, D.N, D.m,
-            D.k, D.s, P.ksub, P.nsub, 0, 1, sl, D.causal ? 1 : 0, stall, status);
+            q, kk, v, D.N, I, W.perm, W.tiles, W.xtl, (int)(units * npc), W.tile_ctr + 1, W.part, W.lse, D.N, D.m,
+            D.k, D.s, P.ksub, P.nsub, npc, 0, 1, sl, D.causal ? 1 : 0, stall, status);
         if ((e = cudaGetLastError())) return e;
         count_launch();
         prof_mark(st, "merge");
