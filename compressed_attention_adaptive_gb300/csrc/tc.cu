@@ -305,7 +305,10 @@ __global__ void __launch_bounds__(320, 1)
     uint8_t* sLo = sm + TILE;
     uint8_t* sK = sm + 2 * TILE;   // NS stages
     uint8_t* sV = sK + NS * TILE;  // NS stages
-    __shared__ uint64_t kv_full[NS], kv_empty[NS], s_full[2], p_full[2], xbar[2];
+    // a stage's keys and values are released separately: K(c) once S(c) is
+    // done, V(c) once O += P V of c is, so the next keys load while the
+    // softmax of c still runs
+    __shared__ uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], p_full[2], xbar[2];
     __shared__ uint64_t pv_done, o_full, q_bar, ebar, drain;
     __shared__ float xmax[2][2][kT], xl[2][kT];
     __shared__ uint32_t tmem_slot;
@@ -320,8 +323,10 @@ __global__ void __launch_bounds__(320, 1)
     if (warp == 9) tmem_alloc(&tmem_slot, 512);
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&kv_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
@@ -357,24 +362,41 @@ __global__ void __launch_bounds__(320, 1)
             // fault test: the first CTA never loads its first chunk, so the MMA
             // warp's bounded wait for it runs out
             const int skip = (stall && mt == 0 && sp == 0 && bh == 0) ? 0 : -1;
-            int issued = 0;
-            for (int c = 0; c < nc; ++c) {
-                const int st = c % NS, use = c / NS;
-                if (!ws_wait(&kv_empty[st], (use & 1) ^ 1, status, abort_v, lim)) break;
-                issued = c + 1;
-                if (c == skip) continue;
-                mbar_expect_tx(&kv_full[st], 2 * TILE);
-                const int y = bh * N + j_begin + c * kT;  // rows past the split are masked, past the end read 0
+            // keys of chunk c go out before values of chunk c - 1: the keys' stage
+            // frees first (S of c - NS completes before O += P V of c - 1 - NS)
+            int issued_k = 0, issued_v = 0;
+            for (int c = 0; c <= nc; ++c) {
+                if (c < nc) {
+                    const int st = c % NS, use = c / NS;
+                    const int y = bh * N + j_begin + c * kT;  // rows past the split are masked, past the end read 0
+                    if (!ws_wait(&k_empty[st], (use & 1) ^ 1, status, abort_v, lim)) break;
+                    issued_k = c + 1;
+                    if (c != skip) {
+                        mbar_expect_tx(&k_full[st], TILE);
 #pragma unroll
-                for (int cb = 0; cb < D / 64; ++cb) {
-                    tma_load_2d(smem_u32(sK + st * TILE) + cb * kT * 128, &tmK, cb * 64, y, &kv_full[st]);
-                    tma_load_2d(smem_u32(sV + st * TILE) + cb * kT * 128, &tmV, cb * 64, y, &kv_full[st]);
+                        for (int cb = 0; cb < D / 64; ++cb)
+                            tma_load_2d(smem_u32(sK + st * TILE) + cb * kT * 128, &tmK, cb * 64, y, &k_full[st]);
+                    }
+                }
+                if (c > 0) {
+                    const int cv = c - 1, st = cv % NS, use = cv / NS;
+                    const int y = bh * N + j_begin + cv * kT;
+                    if (!ws_wait(&v_empty[st], (use & 1) ^ 1, status, abort_v, lim)) break;
+                    issued_v = cv + 1;
+                    if (cv != skip) {
+                        mbar_expect_tx(&v_full[st], TILE);
+#pragma unroll
+                        for (int cb = 0; cb < D / 64; ++cb)
+                            tma_load_2d(smem_u32(sV + st * TILE) + cb * kT * 128, &tmV, cb * 64, y, &v_full[st]);
+                    }
                 }
             }
-            // the loads still in flight (at most the last NS issued) land before
-            // the CTA may exit
-            for (int c = max(0, issued - NS); c < issued; ++c)
-                if (c != skip) drain_wait(&kv_full[c % NS], (c / NS) & 1, status);
+            // the loads still in flight (at most the last NS issued of each kind)
+            // land before the CTA may exit
+            for (int c = max(0, issued_k - NS); c < issued_k; ++c)
+                if (c != skip) drain_wait(&k_full[c % NS], (c / NS) & 1, status);
+            for (int c = max(0, issued_v - NS); c < issued_v; ++c)
+                if (c != skip) drain_wait(&v_full[c % NS], (c / NS) & 1, status);
         }
         __syncwarp();
         cp_async_wait_all();
@@ -385,20 +407,22 @@ __global__ void __launch_bounds__(320, 1)
             fence_proxy_async();  // the landmark tiles came through cp.async (generic proxy)
             auto flush_pv = [&](int h) -> bool {
                 if (!ws_wait(&p_full[h & 1], (h >> 1) & 1, status, abort_v, lim)) return false;
+                if (!ws_wait(&v_full[h % NS], (h / NS) & 1, status, abort_v, lim)) return false;
                 fence_after_sync();
                 issue_pv_ts<D>(tmem + kO, tmem + kS0 + (h & 1) * 128, smem_u32(sV + (h % NS) * TILE), h > 0);
                 mma_commit(&pv_done);
-                mma_commit(&kv_empty[h % NS]);
+                mma_commit(&v_empty[h % NS]);
                 if (h == nc - 1) mma_commit(&o_full);
                 return true;
             };
             for (int c = 0; c < nc && ok; ++c) {
                 const int st = c % NS, sb = c & 1;
-                if (!(ok = ws_wait(&kv_full[st], (c / NS) & 1, status, abort_v, lim))) break;
+                if (!(ok = ws_wait(&k_full[st], (c / NS) & 1, status, abort_v, lim))) break;
                 fence_after_sync();
                 issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sHi), smem_u32(sK + st * TILE), false);
                 issue_qk<D>(tmem + kS0 + sb * 128, smem_u32(sLo), smem_u32(sK + st * TILE), true);
                 mma_commit(&s_full[sb]);
+                mma_commit(&k_empty[st]);
                 if (c > 0 && !(ok = flush_pv(c - 1))) break;
             }
             if (ok) flush_pv(nc - 1);
@@ -1343,35 +1367,35 @@ __global__ void __launch_bounds__(256) k_merge(const __nv_bfloat16* __restrict__
                    pack_bf16(acc[4] * winv, acc[5] * winv), pack_bf16(acc[6] * winv, acc[7] * winv));
 }
 
-// The common case of the merge below (at most kMaxS expert partials and at
-// most one shared partial): every load of a query in flight at once.
-template <int D>
+// The common case of the merge above (S <= kMaxS expert partials, at most
+// one shared partial): every load of a query in flight at once, and no
+// registers held for partials that are not there.
+template <int D, int S>
 __global__ void __launch_bounds__(256) k_merge_few(const __nv_bfloat16* __restrict__ part, const float* __restrict__ lse,
                                                const __nv_bfloat16* __restrict__ sh_part,
                                                const float* __restrict__ sh_lse, __nv_bfloat16* __restrict__ O,
-                                               long long nq, int s) {
+                                               long long nq) {
     constexpr int G = D / 8;  // threads per query
     const long long qi = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / G;
     const int gcol = (threadIdx.x % G) * 8;
     if (qi >= nq) return;
-    float lj[kMaxS + 1];
+    float lj[S + 1];
     float L = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kMaxS; ++j) {
-        lj[j] = j < s ? lse[qi * s + j] : -INFINITY;
+    for (int j = 0; j < S; ++j) {
+        lj[j] = lse[qi * S + j];
         L = fmaxf(L, lj[j]);
     }
-    lj[kMaxS] = sh_part ? sh_lse[qi] : -INFINITY;
-    L = fmaxf(L, lj[kMaxS]);
-    uint4 raw[kMaxS + 1];
+    lj[S] = sh_part ? sh_lse[qi] : -INFINITY;
+    L = fmaxf(L, lj[S]);
+    uint4 raw[S + 1];
 #pragma unroll
-    for (int j = 0; j < kMaxS; ++j)
-        if (j < s) raw[j] = *reinterpret_cast<const uint4*>(part + (qi * s + j) * D + gcol);
-    if (sh_part) raw[kMaxS] = *reinterpret_cast<const uint4*>(sh_part + qi * D + gcol);
+    for (int j = 0; j < S; ++j) raw[j] = *reinterpret_cast<const uint4*>(part + (qi * S + j) * D + gcol);
+    if (sh_part) raw[S] = *reinterpret_cast<const uint4*>(sh_part + qi * D + gcol);
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, wsum = 0.0f;
 #pragma unroll
-    for (int j = 0; j <= kMaxS; ++j) {
-        if (j < kMaxS ? j >= s : !sh_part) continue;
+    for (int j = 0; j <= S; ++j) {
+        if (j == S && !sh_part) continue;
         const float w = lj[j] > -INFINITY ? exp2f(lj[j] - L) : 0.0f;  // an empty partial (causal only) weighs 0
         wsum += w;
         const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
@@ -1386,6 +1410,16 @@ __global__ void __launch_bounds__(256) k_merge_few(const __nv_bfloat16* __restri
     *reinterpret_cast<uint4*>(O + qi * D + gcol) =
         make_uint4(pack_bf16(acc[0] * winv, acc[1] * winv), pack_bf16(acc[2] * winv, acc[3] * winv),
                    pack_bf16(acc[4] * winv, acc[5] * winv), pack_bf16(acc[6] * winv, acc[7] * winv));
+}
+
+template <int D, int S>
+static void launch_merge_few(const TcWork& W, bool shared, void* O, long long nq, unsigned blocks, int ns,
+                             cudaStream_t st) {
+    if constexpr (S < kMaxS) {
+        if (ns > S) return launch_merge_few<D, S + 1>(W, shared, O, nq, blocks, ns, st);
+    }
+    k_merge_few<D, S><<<blocks, 256, 0, st>>>(W.part, W.lse, shared ? W.sh_part : nullptr, W.sh_lse,
+                                              (__nv_bfloat16*)O, nq);
 }
 
 // Producer warps of the expert kernel.
@@ -2232,8 +2266,7 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
         const long long nq = (long long)D.BH * D.N;
         const unsigned mblocks = (unsigned)((nq * (DD / 8) + 255) / 256);
         if (D.s * P.nsub <= kMaxS && P.nsh <= 1)
-            k_merge_few<DD><<<mblocks, 256, 0, st>>>(W.part, W.lse, P.nsh ? W.sh_part : nullptr, W.sh_lse,
-                                                     (__nv_bfloat16*)O, nq, D.s * P.nsub);
+            launch_merge_few<DD, 1>(W, P.nsh > 0, O, nq, mblocks, D.s * P.nsub, st);
         else
             k_merge<DD><<<mblocks, 256, 0, st>>>(W.part, W.lse, D.s * P.nsub, W.sh_part, W.sh_lse, P.nsh,
                                                  (__nv_bfloat16*)O, nq);
