@@ -1015,14 +1015,21 @@ __global__ void __launch_bounds__(320, 1)
                 bi[u] = -1;
             }
             float mx = -INFINITY;
+            [[maybe_unused]] float bv[SMAX];  // SMAX <= 2: the best scores so far, with bi
+            if constexpr (SMAX <= 2) {
+#pragma unroll
+                for (int u = 0; u < SMAX; ++u) bv[u] = -INFINITY;
+            }
 #pragma unroll 1
             for (int c0 = 0; c0 < kT; c0 += 64) {
                 float v[64];
                 tmem_ld32(tR + c0, v);
                 tmem_ld32(tR + c0 + 32, v + 32);
                 tmem_wait_ld();
+                if (m < c0 + 64) {
 #pragma unroll
-                for (int jj = 0; jj < 64; ++jj) v[jj] = c0 + jj < m ? v[jj] : -INFINITY;
+                    for (int jj = 0; jj < 64; ++jj) v[jj] = c0 + jj < m ? v[jj] : -INFINITY;
+                }
                 float bmx = max64(v);
                 if (sl > 0.0f && nsm >= min(m, c0 + 64)) {
                     mx = fmaxf(mx, bmx * sl);
@@ -1030,14 +1037,60 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                     for (int jj = 0; jj < 64; ++jj) mx = fmaxf(mx, c0 + jj < nsm ? v[jj] * sl : -INFINITY);
                 }
-#pragma unroll 1
-                for (int u = 0; u < SMAX; ++u) {
-                    if (!(bmx > -INFINITY) || order_key(bmx) <= bu[SMAX - 1]) break;
-                    const int i = first_eq64(v, bmx);
-                    top_insert<SMAX>(bu, bi, order_key(bmx), c0 + i);
+                if constexpr (SMAX <= 2) {
+                    // one pass over the block in two interleaved chains (even and odd
+                    // columns), each keeping its SMAX best in column order (a strict
+                    // comparison keeps the lower column among equal scores), then
+                    // merged into the row's best by (score, lower column)
+                    float a[2][SMAX];
+                    int ai[2][SMAX];
 #pragma unroll
-                    for (int jj = 0; jj < 64; ++jj) v[jj] = jj == i ? -INFINITY : v[jj];
-                    bmx = max64(v);
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int u = 0; u < SMAX; ++u) {
+                            a[h][u] = -INFINITY;
+                            ai[h][u] = -1;
+                        }
+#pragma unroll
+                    for (int jj = 0; jj < 64; ++jj) {
+                        const int h = jj & 1;
+                        const float x = v[jj];
+                        const bool p1 = x > a[h][0];
+                        if constexpr (SMAX == 2) {
+                            const bool p2 = x > a[h][1];
+                            a[h][1] = p1 ? a[h][0] : (p2 ? x : a[h][1]);
+                            ai[h][1] = p1 ? ai[h][0] : (p2 ? c0 + jj : ai[h][1]);
+                        }
+                        a[h][0] = p1 ? x : a[h][0];
+                        ai[h][0] = p1 ? c0 + jj : ai[h][0];
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int u = 0; u < SMAX; ++u) {
+                            float x = a[h][u];
+                            int xi = ai[h][u];
+#pragma unroll
+                            for (int t = 0; t < SMAX; ++t) {
+                                const bool gt = xi >= 0 && (x > bv[t] || (x == bv[t] && (uint32_t)xi < (uint32_t)bi[t]));
+                                const float tv = bv[t];
+                                const int ti = bi[t];
+                                bv[t] = gt ? x : tv;
+                                bi[t] = gt ? xi : ti;
+                                x = gt ? tv : x;
+                                xi = gt ? ti : xi;
+                            }
+                        }
+                } else {
+#pragma unroll 1
+                    for (int u = 0; u < SMAX; ++u) {
+                        if (!(bmx > -INFINITY) || order_key(bmx) <= bu[SMAX - 1]) break;
+                        const int i = first_eq64(v, bmx);
+                        top_insert<SMAX>(bu, bi, order_key(bmx), c0 + i);
+#pragma unroll
+                        for (int jj = 0; jj < 64; ++jj) v[jj] = jj == i ? -INFINITY : v[jj];
+                        bmx = max64(v);
+                    }
                 }
             }
             // pass 2: the probabilities, P of keys 0..63 over columns 0..31 (scores
