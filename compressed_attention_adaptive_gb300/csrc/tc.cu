@@ -1042,10 +1042,11 @@ __global__ void __launch_bounds__(320, 1)
                     // columns), each keeping its SMAX best in column order (a strict
                     // comparison keeps the lower column among equal scores), then
                     // merged into the row's best by (score, lower column)
-                    float a[2][SMAX];
-                    int ai[2][SMAX];
+                    constexpr int NCH = 2;  // chains
+                    float a[NCH][SMAX];
+                    int ai[NCH][SMAX];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
+                    for (int h = 0; h < NCH; ++h)
 #pragma unroll
                         for (int u = 0; u < SMAX; ++u) {
                             a[h][u] = -INFINITY;
@@ -1053,23 +1054,23 @@ __global__ void __launch_bounds__(320, 1)
                         }
 #pragma unroll
                     for (int jj = 0; jj < 64; ++jj) {
-                        const int h = jj & 1;
+                        const int h = jj % NCH;
                         const float x = v[jj];
                         const bool p1 = x > a[h][0];
                         if constexpr (SMAX == 2) {
                             const bool p2 = x > a[h][1];
                             a[h][1] = p1 ? a[h][0] : (p2 ? x : a[h][1]);
-                            ai[h][1] = p1 ? ai[h][0] : (p2 ? c0 + jj : ai[h][1]);
+                            ai[h][1] = p1 ? ai[h][0] : (p2 ? jj : ai[h][1]);
                         }
                         a[h][0] = p1 ? x : a[h][0];
-                        ai[h][0] = p1 ? c0 + jj : ai[h][0];
+                        ai[h][0] = p1 ? jj : ai[h][0];  // the block's column; c0 added below
                     }
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
+                    for (int h = 0; h < NCH; ++h)
 #pragma unroll
                         for (int u = 0; u < SMAX; ++u) {
                             float x = a[h][u];
-                            int xi = ai[h][u];
+                            int xi = ai[h][u] >= 0 ? c0 + ai[h][u] : -1;
 #pragma unroll
                             for (int t = 0; t < SMAX; ++t) {
                                 const bool gt = xi >= 0 && (x > bv[t] || (x == bv[t] && (uint32_t)xi < (uint32_t)bi[t]));
