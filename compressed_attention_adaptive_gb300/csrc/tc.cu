@@ -1038,11 +1038,11 @@ __global__ void __launch_bounds__(320, 1)
                     for (int jj = 0; jj < 64; ++jj) mx = fmaxf(mx, c0 + jj < nsm ? v[jj] * sl : -INFINITY);
                 }
                 if constexpr (SMAX <= 2) {
-                    // one pass over the block in two interleaved chains (even and odd
-                    // columns), each keeping its SMAX best in column order (a strict
-                    // comparison keeps the lower column among equal scores), then
-                    // merged into the row's best by (score, lower column)
-                    constexpr int NCH = 2;  // chains
+                    // one pass over the block keeping its SMAX best in column order
+                    // (a strict comparison keeps the lower column among equal
+                    // scores), then merged into the row's best by (score, lower
+                    // column); one chain measured faster than interleaved ones
+                    constexpr int NCH = 1;  // chains
                     float a[NCH][SMAX];
                     int ai[NCH][SMAX];
 #pragma unroll
