@@ -35,8 +35,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # a smaller head count scaled to 32 heads. It is tied to the kernel source it
 # was taken on (sha256 of csrc/tc.cu, first 16 hex digits); once that source
 # changes, the figure no longer describes the kernel and the line reports null.
-EXPERT_TRAFFIC = {"kernel": "k_expert_res", "src_sha16": "bd534cca446011b6", "bytes_per_launch": 128.4e6 * 32 / 6,
-                  "how": "ncu dram__bytes.sum of one launch on the 6-head case (128.4 MB), scaled by 32 / 6 heads"}
+EXPERT_TRAFFIC = {"kernel": "k_expert_res", "src_sha16": "cca051e6f4bbed89", "bytes_per_launch": 128.2e6 * 32 / 6,
+                  "how": "ncu dram__bytes.sum of one launch on the 6-head case (128.2 MB), scaled by 32 / 6 heads"}
 
 
 def peaks():
