@@ -347,6 +347,17 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tmem = tmem_slot;
     if (warp == 8) {
         // ------------------------------------------------------- producer
+        // fault test: the first CTA never loads its first chunk, so the MMA
+        // warp's bounded wait for it runs out
+        const int skip = (stall && mt == 0 && sp == 0 && bh == 0) ? 0 : -1;
+        if (lane == 0 && skip != 0) {
+            // the first keys go out before the landmark tiles: their HBM latency
+            // overlaps the tiles' copies (the stage is free: its first use)
+            mbar_expect_tx(&k_full[0], TILE);
+#pragma unroll
+            for (int cb = 0; cb < D / 64; ++cb)
+                tma_load_2d(smem_u32(sK) + cb * kT * 128, &tmK, cb * 64, bh * N + j_begin, &k_full[0]);
+        }
         {
             constexpr int CPR = D / 8, RPI = 32 / CPR;
             const int cc = lane % CPR;
@@ -359,14 +370,11 @@ __global__ void __launch_bounds__(320, 1)
             cp_async_arrive(&q_bar);
         }
         if (lane == 0) {
-            // fault test: the first CTA never loads its first chunk, so the MMA
-            // warp's bounded wait for it runs out
-            const int skip = (stall && mt == 0 && sp == 0 && bh == 0) ? 0 : -1;
             // keys of chunk c go out before values of chunk c - 1: the keys' stage
             // frees first (S of c - NS completes before O += P V of c - 1 - NS)
-            int issued_k = 0, issued_v = 0;
+            int issued_k = 1, issued_v = 0;  // keys of chunk 0: above
             for (int c = 0; c <= nc; ++c) {
-                if (c < nc) {
+                if (c > 0 && c < nc) {
                     const int st = c % NS, use = c / NS;
                     const int y = bh * N + j_begin + c * kT;  // rows past the split are masked, past the end read 0
                     if (!ws_wait(&k_empty[st], (use & 1) ^ 1, status, abort_v, lim)) break;
@@ -537,9 +545,25 @@ __global__ void __launch_bounds__(320, 1)
             if (__all_sync(0xffffffffu, ws_wait(&ebar, 0, status, abort_v, lim))) {
                 const float lt = l + xl[wg ^ 1][r];
                 const size_t orow = ((size_t)bh * splits + sp) * m_pad + row;
-                float* od = Opart + orow * D + wg * DH;
+                // this warp's 32 half rows go through the key/value stages (idle
+                // once O is complete), so that each store writes whole 128-byte
+                // lines: two (d = 128) or four (d = 64) half rows per instruction
+                constexpr int PD = DH + 4;  // padded pitch (floats): conflict-free both ways
+                constexpr int PPR = DH / 4, RPI = 32 / PPR;
+                static_assert(8 * 32 * PD * 4 <= 2 * NS * TILE, "staging fits in the key/value stages");
+                fence_proxy_async();  // the stages were last read by MMAs (async proxy)
+                float* stg = reinterpret_cast<float*>(sK) + (size_t)warp * 32 * PD;
 #pragma unroll
-                for (int j = 0; j < DH; j += 4) *reinterpret_cast<float4*>(od + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+                for (int j = 0; j < DH; j += 4)
+                    *reinterpret_cast<float4*>(stg + lane * PD + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+                __syncwarp();
+                float* od = Opart + (orow - lane) * D + wg * DH;  // this warp's first row
+#pragma unroll
+                for (int i = 0; i < 32 / RPI; ++i) {
+                    const int rl = i * RPI + lane / PPR, u = lane % PPR;
+                    *reinterpret_cast<float4*>(od + (size_t)rl * D + 4 * u) =
+                        *reinterpret_cast<const float4*>(stg + rl * PD + 4 * u);
+                }
                 if (wg == 0) ML[orow] = make_float2(mref, row_ok ? lt : 0.0f);
                 ccount[region] = ncand;
             }
@@ -553,44 +577,47 @@ __global__ void __launch_bounds__(320, 1)
 
 // Merges the per-split partials: Vt = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 // Writes Vt fp32 [BH][m][D] and the bf16 copy [BH][m_pad][D] (padding rows 0).
-// One block per (landmark row, head): D/4 lanes of four columns times SL split
-// lanes, each split lane summing every SL-th split, then a sum over the split
-// lanes in shared memory (the splits run in parallel, so a head split many
-// ways, as few heads are, costs no longer than one split few ways).
+// One block per (landmark row, head): D/4 lanes of four columns times
+// blockDim / (D/4) split lanes (a power of two, about the split count, so a
+// few splits take a small block), each split lane summing every such split,
+// then a sum over the split lanes in shared memory. The splits run in
+// parallel, so a head split many ways, as few heads are, costs no longer than
+// one split few ways.
 template <int D>
 __global__ void __launch_bounds__(256) k_vt_combine(const float* __restrict__ Opart, const float2* __restrict__ ML,
                                                     int splits, int m, int m_pad, float* __restrict__ Vt,
                                                     __nv_bfloat16* __restrict__ Vtb) {
-    constexpr int CG = D / 4, SL = 256 / CG;
-    __shared__ float4 red[SL][CG];
-    __shared__ float rden[SL], wmax[8];
+    constexpr int CG = D / 4, SLMAX = 256 / CG;
+    __shared__ float4 red[SLMAX][CG];
+    __shared__ float rden[SLMAX], wmax[8];
     const int i = blockIdx.x, bh = blockIdx.y;
-    const int cg = threadIdx.x % CG, sl = threadIdx.x / CG;
+    const int cg = threadIdx.x % CG, sl = threadIdx.x / CG, nsl = blockDim.x / CG, nw = blockDim.x >> 5;
+    __nv_bfloat162* vb = reinterpret_cast<__nv_bfloat162*>(Vtb + ((size_t)bh * m_pad + i) * D + 4 * cg);
+    if (i >= m) {  // a padding row: zeros in the bf16 copy only
+        if (sl == 0) vb[0] = vb[1] = __floats2bfloat162_rn(0.0f, 0.0f);
+        return;
+    }
     const size_t o0 = (size_t)bh * splits * m_pad + i;  // ML index of split 0; split s adds s * m_pad
     float M = -INFINITY;
-    if (i < m)
-        for (int s = threadIdx.x; s < splits; s += 256) M = fmaxf(M, ML[o0 + (size_t)s * m_pad].x);
+    for (int s = threadIdx.x; s < splits; s += blockDim.x) M = fmaxf(M, ML[o0 + (size_t)s * m_pad].x);
 #pragma unroll
     for (int x = 16; x >= 1; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
     if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = M;
     __syncthreads();
-#pragma unroll
-    for (int w = 0; w < 8; ++w) M = fmaxf(M, wmax[w]);
+    for (int w = 0; w < nw; ++w) M = fmaxf(M, wmax[w]);
     float4 num = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     float den = 0.0f;
-    if (i < m) {
-        for (int s = sl; s < splits; s += SL) {
-            const size_t o = o0 + (size_t)s * m_pad;
-            const float2 ml = ML[o];
-            if (ml.y == 0.0f) continue;
-            const float w = exp2f(ml.x - M);
-            const float4 v = reinterpret_cast<const float4*>(Opart + o * D)[cg];
-            num.x += w * v.x;
-            num.y += w * v.y;
-            num.z += w * v.z;
-            num.w += w * v.w;
-            den += w * ml.y;
-        }
+    for (int s = sl; s < splits; s += nsl) {
+        const size_t o = o0 + (size_t)s * m_pad;
+        const float2 ml = ML[o];
+        if (ml.y == 0.0f) continue;
+        const float w = exp2f(ml.x - M);
+        const float4 v = reinterpret_cast<const float4*>(Opart + o * D)[cg];
+        num.x += w * v.x;
+        num.y += w * v.y;
+        num.z += w * v.z;
+        num.w += w * v.w;
+        den += w * ml.y;
     }
     red[sl][cg] = num;
     if (cg == 0) rden[sl] = den;
@@ -598,8 +625,7 @@ __global__ void __launch_bounds__(256) k_vt_combine(const float* __restrict__ Op
     if (sl == 0) {
         float4 a = red[0][cg];
         float dd = rden[0];
-#pragma unroll
-        for (int j = 1; j < SL; ++j) {
+        for (int j = 1; j < nsl; ++j) {
             const float4 b = red[j][cg];
             a.x += b.x;
             a.y += b.y;
@@ -607,16 +633,12 @@ __global__ void __launch_bounds__(256) k_vt_combine(const float* __restrict__ Op
             a.w += b.w;
             dd += rden[j];
         }
-        float4 out = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (i < m) {
-            out = make_float4(a.x / dd, a.y / dd, a.z / dd, a.w / dd);
-            float* vt = Vt + ((size_t)bh * m + i) * D + 4 * cg;  // a caller's buffer: 4-byte alignment only
-            vt[0] = out.x;
-            vt[1] = out.y;
-            vt[2] = out.z;
-            vt[3] = out.w;
-        }
-        __nv_bfloat162* vb = reinterpret_cast<__nv_bfloat162*>(Vtb + ((size_t)bh * m_pad + i) * D + 4 * cg);
+        const float4 out = make_float4(a.x / dd, a.y / dd, a.z / dd, a.w / dd);
+        float* vt = Vt + ((size_t)bh * m + i) * D + 4 * cg;  // a caller's buffer: 4-byte alignment only
+        vt[0] = out.x;
+        vt[1] = out.y;
+        vt[2] = out.z;
+        vt[3] = out.w;
         vb[0] = __floats2bfloat162_rn(out.x, out.y);
         vb[1] = __floats2bfloat162_rn(out.z, out.w);
     }
@@ -1021,7 +1043,7 @@ __global__ void __launch_bounds__(320, 1)
                 for (int u = 0; u < SMAX; ++u) bv[u] = -INFINITY;
             }
 #pragma unroll 1
-            for (int c0 = 0; c0 < kT; c0 += 64) {
+            for (int c0 = 0; c0 < m; c0 += 64) {  // blocks past the last landmark hold nothing
                 float v[64];
                 tmem_ld32(tR + c0, v);
                 tmem_ld32(tR + c0 + 32, v + 32);
@@ -2088,11 +2110,25 @@ TcPlan tc_plan(const Dims& D) {
     p.m_pad = (D.m + kT - 1) / kT * kT;
     p.m_tiles = p.m_pad / kT;
     const int nchunks = (D.N + kT - 1) / kT;
-    const long long target = 4LL * 152;  // four CTAs per SM of a GB300
-    long long sp = (target + (long long)D.BH * p.m_tiles - 1) / ((long long)D.BH * p.m_tiles);
-    if (sp < 1) sp = 1;
-    if (sp > 128) sp = 128;  // <= 256 candidate regions per row (two column halves per split) stay stageable
-    if (sp > nchunks) sp = nchunks;
+    // key splits of the landmark pass: one CTA per (landmark tile, split, head),
+    // one CTA per SM, so a launch runs in waves; the split count minimizes
+    // waves x (chunks per split + 3), three chunks' time being about what a
+    // CTA spends outside its chunk loop (start, first loads, epilogue). At most
+    // 128 splits: <= 256 candidate regions per row (two column halves per
+    // split) stay stageable in the selection.
+    long long sp = 1;
+    {
+        long long best_cost = -1;
+        for (long long c = 1; c <= 128 && c <= nchunks; ++c) {
+            const long long cps = (nchunks + c - 1) / c, spl = (nchunks + cps - 1) / cps;
+            const long long waves = ((long long)D.BH * p.m_tiles * spl + num_sms() - 1) / num_sms();
+            const long long cost = waves * (cps + 3);
+            if (best_cost < 0 || cost <= best_cost) {
+                best_cost = cost;
+                sp = c;
+            }
+        }
+    }
     p.chunks_per_split = (int)((nchunks + sp - 1) / sp);
     p.splits = (nchunks + p.chunks_per_split - 1) / p.chunks_per_split;
     p.max_tiles = (long long)D.BH * ((long long)D.N * D.s / kT + D.m + 1);
@@ -2267,7 +2303,11 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
     if (upto >= 2) {
         prof_mark(st, "vt_combine");
         count_launch();
-        k_vt_combine<DD><<<dim3(P.m_pad, D.BH), 256, 0, st>>>(W.Opart, W.ML, P.splits, D.m, P.m_pad, Vt, W.Vtb);
+        // split lanes: a power of two covering the splits, a warp at least, 256 threads at most
+        int vt_threads = DD / 4;
+        while (vt_threads < 256 && (vt_threads < 32 || vt_threads / (DD / 4) < P.splits)) vt_threads *= 2;
+        k_vt_combine<DD><<<dim3(P.m_pad, D.BH), vt_threads, 0, st>>>(W.Opart, W.ML, P.splits, D.m, P.m_pad, Vt,
+                                                                    W.Vtb);
         if ((e = cudaGetLastError())) return e;
     }
     if (!E) return cudaSuccess;

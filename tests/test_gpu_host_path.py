@@ -1,5 +1,7 @@
 """mita_forward_host (host buffers; the copies overlap the compute by groups
-of heads) against mita_forward on the same inputs.
+of heads) against mita_forward on the same inputs. The head counts cover
+groups of one head, groups of two with the last one halved (16 heads: 7 x 2
++ 1 + 1) and of three with an uneven halving (24 heads: 7 x 3 + 2 + 1).
 
 The two results differ only where the head count changes the key splits of
 the shared-expert pass (a different summation order of its partials), so
@@ -15,7 +17,7 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("H", [1, 3, 6])
+@pytest.mark.parametrize("H", [1, 3, 6, 16, 24])
 def test_forward_host_matches_device(H):
     import torch
     import compressed_attention_adaptive_gb300 as mita

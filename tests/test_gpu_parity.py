@@ -40,6 +40,10 @@ SMALL = [
     # (the shared slots' own pass, also in ragged parts)
     L["n131k"].with_(B=1, H=1, N=4096, m=300, k=600, s=3),
     L["longctx_n32k"].with_(B=1, H=2, N=3000, d=64, m=200, k=520, s=2),
+    # one head of the long-context shape: 128 key splits in the landmark pass
+    # (the most the Vt combine sums), one sample chunk per CTA, a block per row
+    # in the sample threshold, experts claimed in pieces
+    L["longctx_n32k"].with_(B=1, H=1),
 ]
 
 
