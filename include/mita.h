@@ -111,7 +111,7 @@ typedef struct {
 /* Bytes of device workspace needed for `p`; 0 if `p` is invalid. On the
  * tensor-core path it holds one bf16 partial output row per (query, routed
  * slot, 256-key sub-expert), so it grows with s * ceil(k / 256): about
- * 2 * B * H * N * d * s * ceil(k / 256) bytes for those rows (2.1 GB in all at
+ * 2 * B * H * N * d * s * ceil(k / 256) bytes for those rows (2.0 GB in all at
  * B2 H16 N32768 d128, m128, k256, s2). */
 size_t mita_workspace_size(const mita_params* p);
 
