@@ -839,7 +839,8 @@ __global__ void __launch_bounds__(320, 1)
     k_route_pp(const __grid_constant__ CUtensorMap tmQ, const __nv_bfloat16* __restrict__ Qhi,
                const __nv_bfloat16* __restrict__ Qlo, const __nv_bfloat16* __restrict__ Vtb, int N, int m, int s,
                int tiles_per_head, int total_tiles, float sl, int causal, int32_t* __restrict__ E,
-               __nv_bfloat16* __restrict__ sh_part, float* __restrict__ sh_lse, int* __restrict__ status) {
+               __nv_bfloat16* __restrict__ sh_part, float* __restrict__ sh_lse, int* __restrict__ counts,
+               int* __restrict__ status) {
     constexpr int TILE = kT * D * 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -1146,7 +1147,12 @@ __global__ void __launch_bounds__(320, 1)
                 int32_t* Erow = E + ((size_t)bh * N + q) * s;
 #pragma unroll
                 for (int u = 0; u < SMAX; ++u)
-                    if (u < s) Erow[u] = bi[u];
+                    if (u < s) {
+                        Erow[u] = bi[u];
+                        // the bucketing's per-(head, expert, slot 0 / later) counts
+                        if (bi[u] < 0 || bi[u] >= m) set_status(status, kStBounds);
+                        else atomicAdd(counts + ((size_t)bh * m + bi[u]) * 2 + (u > 0), 1);
+                    }
             }
             // epilogue: the normalized shared-slot partial row and its log2-sum-exp
             if (!__all_sync(0xffffffffu, ws_wait(&o_full[w], j & 1, status, abort_v))) break;
@@ -2217,7 +2223,7 @@ static cudaError_t launch_route_s(const Dims& D, const TcPlan& P, const TcWork& 
         const int grid = std::min(total, num_sms());
         k_route_pp<DD, SMAX, NSQ><<<grid, 320, smem, st>>>(mq, W.Qhi, W.Qlo, W.Vtb, D.N, D.m, D.s, tph, total,
                                                            D.scale * 1.4426950408889634f, D.causal ? 1 : 0, E,
-                                                           W.sh_part, W.sh_lse, status);
+                                                           W.sh_part, W.sh_lse, W.counts, status);
     } else if (P.m_pad <= 256) {
         const int smem = 2 * P.m_pad * DD * 2 + 2 * tile + 1024;
         if ((e = set_smem(k_route_tc<DD, SMAX>, smem))) return e;
@@ -2311,22 +2317,26 @@ static cudaError_t forward_tc_t(const Dims& D, const TcPlan& P, const TcWork& W,
         if ((e = cudaGetLastError())) return e;
     }
     if (!E) return cudaSuccess;
-    // routing
+    // routing (the routing pass with the shared slots also counts the routes
+    // per expert for the bucketing, into counts cleared here)
     prof_mark(st, "route");
+    if ((e = cudaMemsetAsync(W.zero_begin, 0, W.zero_bytes, st))) return e;
     if ((e = launch_route<DD>(D, P, W, q, E, status, st))) return e;
     if (upto < 2) return cudaSuccess;
     // bucketing
     prof_mark(st, "bucket");
-    if ((e = cudaMemsetAsync(W.zero_begin, 0, W.zero_bytes, st))) return e;
     {
         const int use_smem = D.m <= 4096;
         dim3 grid((D.N + 255) / 256, D.BH);
-        k_bucket_count<<<grid, 256, use_smem ? 8 * D.m : 0, st>>>(E, D.N, D.m, D.s, W.counts, use_smem, status);
+        if (!P.route_shared) {
+            k_bucket_count<<<grid, 256, use_smem ? 8 * D.m : 0, st>>>(E, D.N, D.m, D.s, W.counts, use_smem, status);
+            count_launch();
+        }
         k_bucket_scan<<<D.BH, 512, 0, st>>>(W.counts, D.m, D.N * D.s, W.cursors, W.toff, W.tile_ctr, W.tiles,
                                             W.xtl);
         k_bucket_scatter<<<grid, 256, use_smem ? 8 * D.m : 0, st>>>(E, D.N, D.m, D.s, W.cursors, W.perm, use_smem);
         if ((e = cudaGetLastError())) return e;
-        count_launch(3);
+        count_launch(2);
     }
     // expert attention (and, with more than 128 landmarks, the shared slots) + merge
     {
